@@ -27,12 +27,13 @@ summary of arXiv 2603.23198, and the MarkTechPost-derived news article
 
 Readings where the pages are silent (each listed in the design notes):
   active iff z > 0 in the precision the decision is taken in (NaN, +0 and -0
-  inactive); slots hold active columns in ascending order; slot values are
-  bf16(z) rounded to nearest even; a (row, tile) with more actives than the
-  width W keeps its true count, its first W actives in the slots, and its
-  whole 128-wide slice bf16(ReLU(z)) in a spill list; a row goes to the dense
-  backup iff some tile count exceeds the ELL capacity C; the L1 term adds
-  lambda to dL/dh at active entries.
+  inactive); slots hold active columns in ascending order; slot values are z
+  at the gate accumulator's precision (fp32), since rounding them to bf16
+  alone costs up to ~2% of RMS(y) against the dense definition; a (row,
+  tile) with more actives than the width W keeps its true count, its first W
+  actives in the slots, and its whole 128-wide fp32 slice ReLU(z) in a spill
+  list; a row goes to the dense backup iff some tile count exceeds the ELL
+  capacity C; the L1 term adds lambda to dL/dh at active entries.
 
 Parity pins: every function here is checked in ``tests/test_oracle_*.py``
 against hand-derived fixtures (``tests/golden/``), brute-force loops on tiny
@@ -146,8 +147,8 @@ class TwELL:
 
     cnt  [T][n_t]     number of active entries of row t in column tile k
     col  [T][n_t][W]  local column (0..tile-1) of slot s, valid for s < min(cnt, W)
-    val  [T][n_t][W]  bf16 bits of z at that column
-    spill  dict (t, k) -> [tile] bf16 bits of ReLU(z) for every (t, k) with cnt > W
+    val  [T][n_t][W]  fp32 z at that column
+    spill  dict (t, k) -> [tile] fp32 ReLU(z) for every (t, k) with cnt > W
     """
     T: int
     F: int
@@ -170,8 +171,8 @@ def twell_pack(z, tile, width):
     decision is taken in (fp32 from a kernel, or fp64).  For every row t and
     column tile k = [k*tile, (k+1)*tile): list the columns with z > 0 in
     ascending order; cnt is the list's length; the first min(cnt, W) go to
-    the slots with value bf16(z); if cnt > W the whole slice bf16(ReLU(z)) is
-    kept in the spill list.
+    the slots with value z (fp32); if cnt > W the whole slice ReLU(z) (fp32)
+    is kept in the spill list.
     """
     z = np.asarray(z)
     T, F = z.shape
@@ -184,19 +185,18 @@ def twell_pack(z, tile, width):
     # stable sort puts the active columns first, in ascending order
     order = np.argsort(~act, axis=2, kind="stable")
     col = np.zeros((T, n_t, width), np.int64)
-    val = np.zeros((T, n_t, width), np.uint16)
+    val = np.zeros((T, n_t, width), np.float32)
     take = min(width, tile)
     col[:, :, :take] = order[:, :, :take]
-    bits = f32_to_bf16(zt)
-    val[:, :, :take] = np.take_along_axis(bits, order[:, :, :take], axis=2)
+    val[:, :, :take] = np.take_along_axis(zt, order[:, :, :take], axis=2)
     s = np.arange(width)[None, None, :]
     valid = s < np.minimum(cnt, width)[:, :, None]
     col = np.where(valid, col, 0)
-    val = np.where(valid, val, 0).astype(np.uint16)
+    val = np.where(valid, val, np.float32(0)).astype(np.float32)
     spill = {}
-    relu_bits = f32_to_bf16(np.where(act, zt, np.float32(0.0)))
+    relu = np.where(act, zt, np.float32(0.0)).astype(np.float32)
     for t, k in zip(*np.nonzero(cnt > width)):
-        spill[(int(t), int(k))] = relu_bits[t, k].copy()
+        spill[(int(t), int(k))] = relu[t, k].copy()
     return TwELL(T, F, tile, width, cnt, col, val, spill)
 
 
@@ -207,7 +207,7 @@ def twell_pack_loops(z, tile, width):
     n_t = F // tile
     cnt = np.zeros((T, n_t), np.int64)
     col = np.zeros((T, n_t, width), np.int64)
-    val = np.zeros((T, n_t, width), np.uint16)
+    val = np.zeros((T, n_t, width), np.float32)
     spill = {}
     for t in range(T):
         for k in range(n_t):
@@ -217,20 +217,19 @@ def twell_pack_loops(z, tile, width):
                 if v > 0:
                     if c < width:
                         col[t, k, c] = j
-                        val[t, k, c] = f32_to_bf16(np.array([v]))[0]
+                        val[t, k, c] = v
                     c += 1
             cnt[t, k] = c
             if c > width:
-                sl = np.array([z[t, k * tile + j] if z[t, k * tile + j] > 0 else 0.0
-                               for j in range(tile)], np.float32)
-                spill[(t, k)] = f32_to_bf16(sl)
+                spill[(t, k)] = np.array([z[t, k * tile + j] if z[t, k * tile + j] > 0 else 0.0
+                                          for j in range(tile)], np.float32)
     return TwELL(T, F, tile, width, cnt, col, val, spill)
 
 
 def twell_unpack(tw: TwELL):
-    """Dense [T][F] bf16 bits of the gate activation rebuilt from slots and
-    spill.  unpack(pack(z)) equals bf16(ReLU(z)) exactly."""
-    h = np.zeros((tw.T, tw.n_t, tw.tile), np.uint16)
+    """Dense [T][F] fp32 gate activation rebuilt from slots and spill.
+    unpack(pack(z)) equals ReLU(z) (fp32) exactly."""
+    h = np.zeros((tw.T, tw.n_t, tw.tile), np.float32)
     s = np.arange(tw.width)[None, None, :]
     in_slots = (s < tw.cnt[:, :, None]) & (tw.cnt <= tw.width)[:, :, None]
     t_i, k_i, s_i = np.nonzero(in_slots)
@@ -241,8 +240,9 @@ def twell_unpack(tw: TwELL):
 
 
 def twell_entries(tw: TwELL, t):
-    """(global column, bf16 bits) of every stored active entry of row t, in
-    ascending column order, taken from slots or the spill slice."""
+    """(global column, fp32 value) of every stored active entry of row t, in
+    ascending column order, taken from slots or the spill slice (a spill
+    slice entry is active iff its value is > 0)."""
     out = []
     for k in range(tw.n_t):
         c = int(tw.cnt[t, k])
@@ -250,11 +250,11 @@ def twell_entries(tw: TwELL, t):
         if c > tw.width:
             sl = tw.spill[(t, k)]
             for j in range(tw.tile):
-                if sl[j] != 0:
-                    out.append((base + j, int(sl[j])))
+                if sl[j] > 0:
+                    out.append((base + j, float(sl[j])))
         else:
             for s in range(c):
-                out.append((base + int(tw.col[t, k, s]), int(tw.val[t, k, s])))
+                out.append((base + int(tw.col[t, k, s]), float(tw.val[t, k, s])))
     return out
 
 
@@ -262,7 +262,7 @@ def ffn_forward_twell(x, tw: TwELL, Wu_t, Wd, rows=None):
     """Fused up+down projection driven by a TwELL gate (paper section
     2.B.2): for each row t and each stored nonzero (j, h):
     u = x_t . W_u[:, j]; y_t += (h u) W_d[j, :].  fp64 arithmetic on the
-    stored bf16 h values.  Returns y for ``rows`` (default all)."""
+    stored fp32 h values.  Returns y for ``rows`` (default all)."""
     X = bf16_to_f64(x)
     U = bf16_to_f64(Wu_t)
     Dn = bf16_to_f64(Wd)
@@ -274,7 +274,7 @@ def ffn_forward_twell(x, tw: TwELL, Wu_t, Wd, rows=None):
         if not ent:
             continue
         js = np.array([e[0] for e in ent])
-        hs = bf16_to_f64(np.array([e[1] for e in ent], np.uint16))
+        hs = np.array([e[1] for e in ent], np.float64)
         u = U[js] @ X[t]
         y[i] = (hs * u) @ Dn[js]
     return y
@@ -292,8 +292,8 @@ class Hybrid:
     ell_rows   ascending token indices of the ELL part
     dense_rows ascending token indices of the dense backup
     row_map    [T]: i >= 0 -> ELL row i; i < 0 -> dense row -(i+1)
-    ell_cnt    [n_ell][n_t], ell_col / ell_val [n_ell][n_t][C]
-    dense_h    [n_dense][F] bf16 bits of ReLU(z)
+    ell_cnt    [n_ell][n_t], ell_col / ell_val [n_ell][n_t][C] (fp32 values)
+    dense_h    [n_dense][F] fp32 ReLU(z)
     """
     T: int
     F: int
@@ -322,7 +322,7 @@ def to_hybrid(tw: TwELL, cap):
     n_t = tw.n_t
     ell_cnt = tw.cnt[ell_rows].copy()
     ell_col = np.zeros((len(ell_rows), n_t, cap), np.int64)
-    ell_val = np.zeros((len(ell_rows), n_t, cap), np.uint16)
+    ell_val = np.zeros((len(ell_rows), n_t, cap), np.float32)
     # entries held in the TwELL slots (count <= W) ...
     m = min(cap, tw.width)
     s = np.arange(m)[None, None, :]
@@ -333,7 +333,7 @@ def to_hybrid(tw: TwELL, cap):
     for i, t in enumerate(ell_rows):
         for k in np.nonzero(ell_cnt[i] > tw.width)[0]:
             sl = tw.spill[(int(t), int(k))]
-            js = np.nonzero(sl)[0]
+            js = np.nonzero(sl > 0)[0]
             ell_col[i, k, :len(js)] = js
             ell_val[i, k, :len(js)] = sl[js]
     full = twell_unpack(tw)
