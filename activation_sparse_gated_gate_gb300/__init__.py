@@ -1,0 +1,176 @@
+"""Python binding of libtwell.so, the GB300 (sm_103a) activation-sparse gated
+FFN library with the TwELL format.
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  torch supplies device memory and streams.  The
+functions keep the C entry points' names (see ``include/twell.h``); they take
+torch tensors, pass their device pointers, and raise ``TwellError`` when the
+C call returns an error.  There is no fallback: if ``libtwell.so`` has not
+been built, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TwellError", "TwELL", "lib", "twell_gate_pack", "twell_ffn_fwd", "twell_status_string",
+    "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "TILE",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtwell.so")
+TILE = 128
+FLAG_SPILL_FULL = 1
+FLAG_DENSE_FULL = 2
+FLAG_TIMEOUT = 4
+
+c_i32 = ctypes.c_int32
+c_ptr = ctypes.c_void_p
+
+
+class TwellStruct(ctypes.Structure):
+    """Mirror of ``twell_t``."""
+    _fields_ = [
+        ("T", c_i32), ("F", c_i32), ("tile", c_i32), ("width", c_i32),
+        ("val", c_ptr), ("col", c_ptr), ("cnt", c_ptr), ("spill_slot", c_ptr),
+        ("spill_cap", c_i32), ("spill_n", c_ptr), ("spill_rt", c_ptr), ("spill_val", c_ptr),
+    ]
+
+
+class TwellError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {twell_status_string(code)}")
+
+
+_LIB = None
+
+# name -> (restype, argtypes)
+_SIGNATURES = {
+    "twell_gate_pack": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_i32, ctypes.POINTER(TwellStruct),
+                                c_ptr, c_ptr, c_ptr]),
+    "twell_ffn_fwd": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
+                              c_ptr, c_ptr]),
+    "twell_status_string": (ctypes.c_char_p, [c_i32]),
+    "twell_version": (c_i32, []),
+}
+
+
+def lib():
+    """The loaded ``libtwell.so`` (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m activation_sparse_gated_gate_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def twell_status_string(code: int) -> str:
+    return lib().twell_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, where):
+    if code != 0:
+        raise TwellError(code, where)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class TwELL:
+    """Device buffers of a TwELL gate activation and the ``twell_t``
+    descriptor that points at them (layouts in ``include/twell.h``).
+
+    ``spill_cap`` defaults to T * n_t slices, enough for every (row, tile)
+    to overflow.  ``status`` is a device int32 the kernels OR flags into.
+    """
+
+    def __init__(self, T: int, F: int, width: int, spill_cap: int | None = None,
+                 device=None, tile: int = TILE):
+        device = torch.device(device if device is not None else "cuda")
+        n_t = F // tile
+        if spill_cap is None:
+            spill_cap = T * n_t if width < tile else 0
+        self.T, self.F, self.width, self.tile, self.n_t = T, F, width, tile, n_t
+        self.spill_cap = spill_cap
+        self.device = device
+        self.val = torch.empty((T, n_t, width), dtype=torch.float32, device=device)
+        self.col = torch.empty((T, n_t, width), dtype=torch.uint8, device=device)
+        self.cnt = torch.empty((T, n_t), dtype=torch.uint8, device=device)
+        self.spill_slot = torch.empty((T, n_t), dtype=torch.int32, device=device)
+        self.spill_n = torch.zeros((1,), dtype=torch.int32, device=device)
+        self.spill_rt = torch.empty((max(spill_cap, 1),), dtype=torch.int32, device=device)
+        self.spill_val = torch.empty((max(spill_cap, 1), tile), dtype=torch.float32,
+                                     device=device)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+        self.struct = TwellStruct(
+            T, F, tile, width, self.val.data_ptr(), self.col.data_ptr(), self.cnt.data_ptr(),
+            self.spill_slot.data_ptr(), spill_cap, self.spill_n.data_ptr(),
+            self.spill_rt.data_ptr(), self.spill_val.data_ptr())
+
+
+def twell_gate_pack(x, Wg_t, out: TwELL, z_debug=None, status=None, stream=None):
+    """Gate GEMM z = x W_g with the TwELL-packing epilogue into ``out``.
+    ``z_debug`` (optional [T][F] fp32) receives z."""
+    _need(x, torch.bfloat16, "x")
+    _need(Wg_t, torch.bfloat16, "Wg_t")
+    if z_debug is not None:
+        _need(z_debug, torch.float32, "z_debug")
+    status = out.status if status is None else status
+    T, D = x.shape
+    F = Wg_t.shape[0]
+    if Wg_t.shape[1] != D:
+        raise ValueError("Wg_t must be [F][D]")
+    with torch.cuda.device(x.device):
+        _check(lib().twell_gate_pack(_ptr(x), _ptr(Wg_t), T, D, F, ctypes.byref(out.struct),
+                                     _ptr(z_debug), _ptr(status), _stream(stream)),
+               "twell_gate_pack")
+    return out
+
+
+def twell_ffn_fwd(x, h: TwELL, Wu_t, Wd, y=None, status=None, stream=None):
+    """Fused up + down projection from the TwELL gate ``h``; returns y
+    [T][D] fp32 (allocated if not given)."""
+    _need(x, torch.bfloat16, "x")
+    _need(Wu_t, torch.bfloat16, "Wu_t")
+    _need(Wd, torch.bfloat16, "Wd")
+    T, D = x.shape
+    if y is None:
+        y = torch.empty((T, D), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, "y")
+    if Wu_t.shape != (h.F, D) or Wd.shape != (h.F, D) or T != h.T:
+        raise ValueError("shape mismatch: x [T][D], Wu_t and Wd [F][D]")
+    status = h.status if status is None else status
+    with torch.cuda.device(x.device):
+        _check(lib().twell_ffn_fwd(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
+                                   _ptr(y), _ptr(status), _stream(stream)),
+               "twell_ffn_fwd")
+    return y

@@ -1,0 +1,325 @@
+"""Benchmark of the activation-sparse gated FFN (TwELL) inference step on GB300.
+
+One step = one pass of the inference hot path over one batch: the gate GEMM
+with the TwELL-packing epilogue (twell_gate_pack) followed by the fused
+up+down projection (twell_ffn_fwd).  Default workload: the 0.5B-class layer,
+T=8192 tokens, d_model=1536, d_ff=6144, ~1% active gate neurons, TwELL width
+8 (seeded synthetic inputs, see workloads.py).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Timing: W warm-up steps, then K timed steps.  Before every timed step a
+512 MiB buffer is written to flush the 129 MB L2; each step is bracketed by
+CUDA events on the launching stream (the flush is outside them), and the
+per-kernel times come from events around each kernel.  Multi-GPU runs (one
+process per GPU under torchrun) are replicas: each rank runs the full batch,
+and the job value is all ranks' tokens over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of roofline"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_step(w, rows):
+    import oracle
+    x = w.x[rows]
+    z = oracle.gate_preact(x, w.Wg_t)
+    tw = oracle.twell_pack(z, 128, w.width)
+    return oracle.ffn_forward_twell(x, tw, w.Wu_t, w.Wd)
+
+
+def time_oracle(w, budget_s=10.0, chunk=64, seed=0):
+    """Tokens/s of the oracle's inference path on sampled rows, run for about
+    `budget_s` seconds of host CPU (at least one chunk)."""
+    rng = np.random.default_rng(seed)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        rows = np.sort(rng.choice(w.T, size=min(chunk, w.T), replace=False))
+        oracle_step(w, rows)
+        done += len(rows)
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el, done, el
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_step(w, np.arange(min(16, w.T)))
+    vals = []
+    tot_rows = 0
+    tot_s = 0.0
+    for _ in range(args.steps):
+        v, n, s = time_oracle(w, budget_s=args.ref_budget)
+        vals.append(v)
+        tot_rows += n
+        tot_s += s
+    value = tot_rows / tot_s
+    cores = os.cpu_count()
+    sample = (f"{tot_rows} sampled token rows of {w.name} over {args.steps} steps "
+              f"(gate fp64 matmul + TwELL pack + fused up/down in fp64)")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * w.T / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F,
+                   "twell_width": w.width, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU path
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import activation_sparse_gated_gate_gb300 as tw
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    def up(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    x, Wg, Wu, Wd = up(w.x), up(w.Wg_t), up(w.Wu_t), up(w.Wd)
+    h = tw.TwELL(w.T, w.F, w.width, device=dev)
+    y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        tw.twell_gate_pack(x, Wg, h, stream=stream)
+        tw.twell_ffn_fwd(x, h, Wu, Wd, y=y, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(h.status.item()) != 0:
+        raise RuntimeError(f"device status flags {int(h.status.item())}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            tw.twell_gate_pack(x, Wg, h, stream=stream)
+            ev[i][1].record(stream)
+            tw.twell_ffn_fwd(x, h, Wu, Wd, y=y, stream=stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t_k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = sum(a + b for a, b in zip(t_k1, t_k2))
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / K
+    value = ws * w.T / (total_ms / K / 1e3)
+
+    # end to end through the public API with host buffers: pinned x in, y out
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(y, device="cpu").pin_memory()
+    e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        e_ev[i][0].record(stream)
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e_ev) / K
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = x.numel() * 2
+    d2h = y.numel() * 4
+
+    hbm, bf16, bf16_sus, src = _peaks()
+    k1_ms = statistics.mean(t_k1)
+    k2_ms = statistics.mean(t_k2)
+    nnz = int(h.cnt.to(torch.int64).sum().item())
+    k1_flops = 2.0 * w.T * w.D * w.F
+    k1_tf = k1_flops / (k1_ms * 1e-3) / 1e12
+    # fused kernel: algorithmic bytes = x in (bf16) + y out (fp32) + W_u/W_d
+    # rows of every neuron (all are active in some row at these sizes) + the
+    # TwELL entries read (5 B per nnz: fp32 value + u8 column, 1 B per count)
+    k2_bytes = w.T * w.D * (2 + 4) + w.F * w.D * 2 * 2 + 5 * nnz + w.T * (w.F // 128)
+    k2_gbs = k2_bytes / (k2_ms * 1e-3) / 1e9
+    kernels = {
+        "twell_gate_pack": {"ms": k1_ms, "tflops": k1_tf, "frac_bf16": k1_tf / bf16},
+        "twell_ffn_fwd": {"ms": k2_ms, "gbs": k2_gbs, "frac_hbm": k2_gbs / hbm,
+                          "flops": 4.0 * w.D * nnz},
+    }
+    if k1_ms >= k2_ms:
+        roof = {"kernel": "twell_gate_pack", "bound": "tensor", "achieved": k1_tf,
+                "peak": bf16, "unit": "TFLOP/s", "frac": k1_tf / bf16,
+                "peak_source": f"{src} bf16 burst", "traffic": None}
+    else:
+        roof = {"kernel": "twell_ffn_fwd", "bound": "hbm", "achieved": k2_gbs, "peak": hbm,
+                "unit": "GB/s", "frac": k2_gbs / hbm, "peak_source": f"{src} HBM copy",
+                "traffic": None}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F,
+                   "twell_width": w.width, "nnz": nnz,
+                   "density": nnz / (w.T * w.F), "l2": "flushed (512 MiB write) before every step",
+                   "parallelism": f"replicas x{ws}"},
+        "e2e": {"value": ws * w.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * K,
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, n, s = time_oracle(w, budget_s=args.ref_budget)
+        out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
+                               "kind": "oracle",
+                               "sample": f"{n} sampled token rows in {s:.1f} s (fp64 oracle)"}
+    if rank == 0:
+        print(json.dumps(out))
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    import workloads
+    w = workloads.config(args.config)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

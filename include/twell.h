@@ -1,0 +1,148 @@
+/*
+ * twell.h - C ABI of the GB300 (sm_103a) activation-sparse gated FFN library.
+ *
+ * The library computes the gated feed-forward block of a ReLU Transformer,
+ *     z = x W_g,   h = ReLU(z),   u = x W_u,   y = (h * u) W_d,
+ * with the gate activation h held in TwELL (Tile-wise ELLPACK), and the
+ * training step over the hybrid (ELL + dense backup) format.
+ *
+ * Sources ("Sparser, Faster, Lighter Transformer Language Models", summary
+ * at gist.science, and the news article "Sakana AI and NVIDIA TwELL boosts
+ * LLM training speed by 21.9%"):
+ *   - ReLU replaces SiLU so the gate has exact zeros; an L1 term with
+ *     coefficient 2e-5 on the FFN activations (news article, recipe list;
+ *     paper section 2.A).
+ *   - TwELL splits the gate columns into horizontal tiles the width of the
+ *     matmul tile and is written in the epilogue of the gate matmul
+ *     h_g = ReLU(x W_g), with no separate conversion kernel (paper section
+ *     2.B.1; news article, epilogue paragraph).
+ *   - One fused kernel does the up and down projections from the TwELL gate,
+ *     computing dot products only for nonzeros (paper section 2.B.2).
+ *   - Training converts TwELL to a hybrid format (compact ELL rows plus a
+ *     dense backup for overflow rows) and runs sparse-to-dense and
+ *     dense-to-sparse matmuls forward and backward (paper section 2.B.3).
+ *
+ * Conventions (every entry point):
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Pointers are device
+ *     pointers unless stated otherwise.  The caller owns all memory; the
+ *     library allocates nothing and never synchronises: all work is enqueued
+ *     on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *   - Weights are stored neuron-major, [F][D] row-major: Wg_t = W_g^T,
+ *     Wu_t = W_u^T, Wd = W_d.  Activations x, y are [T][D] row-major.
+ *   - Arguments are validated on the host before anything is enqueued.  A
+ *     failure returns TWELL_ERR_INVALID (or TWELL_ERR_UNSUPPORTED) and
+ *     enqueues nothing.  TWELL_ERR_CUDA means a CUDA call failed while
+ *     enqueuing; cudaGetLastError() then holds the CUDA error.
+ *   - Data-dependent conditions found on the device (a full spill list, a
+ *     full dense backup, a wait that timed out) never trap: the kernels OR a
+ *     TWELL_FLAG_* bit into *status_dev (a caller-owned device int32 the
+ *     library never clears) and the outputs of the affected rows are then
+ *     undefined.  Read it after synchronising the stream.
+ *   - Alignment: every pointer 16-byte aligned; D % 8 == 0 (rows of 16-byte
+ *     multiples); F % 128 == 0; tile == 128.
+ */
+#ifndef TWELL_H
+#define TWELL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TWELL_OK = 0,
+  TWELL_ERR_INVALID = 1,      /* bad argument; nothing enqueued */
+  TWELL_ERR_UNSUPPORTED = 2,  /* device is not sm_103 or a size limit is exceeded */
+  TWELL_ERR_CUDA = 3          /* a CUDA runtime call failed while enqueuing */
+} twell_status;
+
+/* Bits OR-ed into *status_dev by the kernels. */
+enum {
+  TWELL_FLAG_SPILL_FULL = 1,  /* more (row, tile) slices overflowed W than spill_cap */
+  TWELL_FLAG_DENSE_FULL = 2,  /* more overflow rows than the hybrid's max_dense */
+  TWELL_FLAG_TIMEOUT = 4      /* a pipeline wait exceeded its bound (about 1 s) */
+};
+
+#define TWELL_TILE 128
+
+/*
+ * TwELL gate activation of a [T][F] matrix (paper section 2.B.1).
+ * n_t = F / tile column tiles.  For row t and tile k (columns
+ * [k*tile, (k+1)*tile)):
+ *   cnt[t*n_t + k]            number of active entries (z > 0), 0..tile
+ *   col[(t*n_t + k)*W + s]    local column of slot s (ascending), s < min(cnt, W)
+ *   val[(t*n_t + k)*W + s]    z at that column, fp32 (the accumulator's value)
+ * Slots at or beyond min(cnt, W) are not written and hold anything.
+ * When cnt > W the (row, tile) keeps its first W actives in the slots and its
+ * whole fp32 slice ReLU(z) (tile values) in the spill list:
+ *   spill_slot[t*n_t + k]     index of that slice, meaningful only where cnt > W;
+ *                             an index >= spill_cap means the list was full
+ *   spill_rt[s]               t*n_t + k of slice s
+ *   spill_val[s*tile + c]     fp32 ReLU(z) of column k*tile + c
+ *   *spill_n                  slices requested by the last pack (device int32;
+ *                             may exceed spill_cap, then TWELL_FLAG_SPILL_FULL)
+ * Sizes: val [T][n_t][W] float, col [T][n_t][W] uint8, cnt [T][n_t] uint8,
+ * spill_slot [T][n_t] int32, spill_rt [spill_cap] int32,
+ * spill_val [spill_cap][tile] float.  spill_* may be NULL when spill_cap = 0.
+ * (The pages leave the value precision open; fp32 keeps the stored gate
+ * exact to the accumulator, where bf16 alone would cost up to ~2% of RMS(y).)
+ */
+typedef struct {
+  int32_t T;          /* rows (tokens) */
+  int32_t F;          /* columns (d_ff), a multiple of tile */
+  int32_t tile;       /* column tile width; must be TWELL_TILE */
+  int32_t width;      /* W: slots per (row, tile), 1..tile */
+  float* val;
+  uint8_t* col;
+  uint8_t* cnt;
+  int32_t* spill_slot;
+  int32_t spill_cap;
+  int32_t* spill_n;
+  int32_t* spill_rt;
+  float* spill_val;
+} twell_t;
+
+/*
+ * Gate GEMM with the TwELL epilogue (paper section 2.B.1; news article,
+ * epilogue paragraph): z = x W_g with fp32 accumulation on the tensor cores,
+ * then, in the same kernel, every (row, tile) slice of z is packed into
+ * `*out`.  No dense h is written.
+ *   x        [T][D] bf16            Wg_t  [F][D] bf16 (= W_g^T)
+ *   out      TwELL with out->T == T, out->F == F; the kernel resets
+ *            *out->spill_n to 0 first (stream-ordered)
+ *   z_debug  optional [T][F] fp32 copy of z (NULL to skip), for checking
+ *   status_dev  device int32, see TWELL_FLAG_*
+ * T may be 0 (nothing enqueued).
+ */
+twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T, int32_t D,
+                             int32_t F, const twell_t* out, float* z_debug,
+                             int32_t* status_dev, void* stream);
+
+/*
+ * Fused up + down projection from a TwELL gate (paper section 2.B.2): for
+ * each row t and each stored active entry (j, h), u = x_t . W_u[:, j]
+ * (fp32), and y_t += (h u) W_d[j, :] (fp32 accumulation).  Rows with no
+ * active entry get y_t = 0.
+ *   x   [T][D] bf16, T = h->T      Wu_t, Wd  [F][D] bf16, F = h->F
+ *   y   [T][D] fp32 (written; fp32 because a bf16 output alone can exceed a
+ *       2e-2 * RMS(y) error where |y| reaches 10 * RMS)
+ * A (row, tile) whose spill slice is missing (index >= spill_cap) is skipped
+ * and TWELL_FLAG_SPILL_FULL is set.
+ */
+twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
+                           const uint16_t* Wd, int32_t D, float* y, int32_t* status_dev,
+                           void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* twell_status_string(twell_status s);
+
+/* Library version, (major << 16) | minor. */
+int32_t twell_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TWELL_H */
