@@ -3,18 +3,34 @@
 // up and down projections from the TwELL gate activations, computing dot
 // products only for the nonzero elements and keeping DRAM traffic low).
 //
-// One warp per token row t.  x_t and the fp32 accumulator of y_t live in
-// registers, spread over the 32 lanes in 16-byte chunks (lane l holds chunks
-// l, l+32, ...).  The warp walks the row's TwELL tiles (the counts of 32
-// tiles are read at once and the non-empty ones found with a ballot); for
-// every active (j, h) it gathers neuron j's rows W_u^T[j] and W_d[j] (2*D
-// contiguous bf16 each, 16-byte vector loads, coalesced across the warp),
-// forms u = x_t . W_u[:, j] with a butterfly reduction and accumulates
-// (h u) W_d[j, :] in fp32.
+// Work unit = (token row t, range of G column tiles); one warp per unit at a
+// time (8 warps per CTA, one CTA per SM, units strided over the grid).  With
+// many tokens G covers the whole row and the warp stores y_t; with few
+// tokens (decode) rows are split into several units so every SM gets work,
+// and each unit adds its partial y_t with 16-byte atomics into a zeroed y.
+// x_t (fp32) and the fp32 accumulator of y_t live in registers, spread over
+// the 32 lanes in 8-element chunks (lane l holds chunks l, l+32, ...).
+//
+// Per unit the warp first lists its active entries (j, h) in shared memory:
+// the counts of 32 tiles are read at once, a warp prefix sum places every
+// tile's entries, and each lane copies its tile's slots (or scans its spill
+// slice).  The warp then walks the list through a ring of P shared-memory
+// stages: lane 0 issues two cp.async.bulk copies per entry (neuron j's rows
+// W_u^T[j] and W_d[j], 2*D contiguous bf16 each) completing on the stage's
+// mbarrier, P entries ahead of the compute.  Per entry the lanes read the
+// staged rows with 16-byte shared loads, form u = x_t . W_u[:, j] with four
+// independent partial sums and a butterfly reduction, and accumulate
+// (h u) W_d[j, :].
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace twell {
 namespace {
+
+constexpr int kWarps = 8;
+constexpr int kListCap = 256;        // entries listed per pass
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 220 * 1024;
 
 struct FfnParams {
   const uint16_t* x;
@@ -28,161 +44,252 @@ struct FfnParams {
   const float* spill_val;
   int32_t spill_cap;
   int32_t T, D, n_t, W;
+  int32_t G;           // column tiles per work unit
+  int32_t upr;         // units per token row, ceil(n_t / G)
+  int32_t split;       // rows split over several units: accumulate with atomics
+  int32_t stages;      // P
+  int32_t warp_bytes;  // shared memory per warp
   int32_t* status;
+};
+
+struct Entry {
+  int32_t j;
+  float h;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-// NC = 16-byte chunks per lane (D <= 256 * NC).  EXACT: D == 256 * NC, so
-// every lane owns every one of its chunks and no predicate is needed.
+// NC = 8-element chunks per lane (D <= 256 * NC).  EXACT: D == 256 * NC, so
+// every lane owns all NC of its chunks.
 template <int NC, bool EXACT>
-struct RowState {
-  uint32_t x[NC][4];   // x_t, bf16 pairs
-  float acc[NC][8];    // y_t accumulator
-
-  __device__ __forceinline__ bool own(int i, int lane, int nch) const {
-    return EXACT || (lane + 32 * i) < nch;
-  }
-
-  // u = x_t . W_u[:, j];  y_t += (h u) W_d[j, :]
-  __device__ __forceinline__ void nonzero(const FfnParams& p, int j, float h, int lane,
-                                          int nch) {
-    const uint16_t* wu = p.Wu_t + static_cast<size_t>(j) * p.D;
-    const uint16_t* wd = p.Wd + static_cast<size_t>(j) * p.D;
-    uint4 a[NC], b[NC];
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-      if (own(i, lane, nch)) {
-        a[i] = ldg16(wu + 8 * (lane + 32 * i));
-        b[i] = ldg16(wd + 8 * (lane + 32 * i));
-      } else {
-        a[i] = make_uint4(0, 0, 0, 0);
-        b[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    float part = 0.0f;
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-      const uint32_t av[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        part = fmaf(bf16lo(x[i][e]), bf16lo(av[e]), part);
-        part = fmaf(bf16hi(x[i][e]), bf16hi(av[e]), part);
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    const float s = h * part;
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-      const uint32_t bv[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc[i][2 * e] = fmaf(s, bf16lo(bv[e]), acc[i][2 * e]);
-        acc[i][2 * e + 1] = fmaf(s, bf16hi(bv[e]), acc[i][2 * e + 1]);
-      }
-    }
-  }
-};
-
-template <int NC, bool EXACT>
-__global__ void __launch_bounds__(256) ffn_fwd_kernel(const FfnParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int nch = p.D >> 3;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < p.T; t += warps) {
-    RowState<NC, EXACT> st;
-    const uint16_t* xr = p.x + static_cast<size_t>(t) * p.D;
+  const int wid = threadIdx.x >> 5;
+  const int P = p.stages;
+  const int D = p.D;
+  const int nch = D >> 3;
+  const uint32_t row_bytes = static_cast<uint32_t>(D) * 2u;
+
+  uint8_t* wbase = smem + static_cast<size_t>(wid) * p.warp_bytes;
+  uint8_t* stages = wbase;                                   // P x [W_u row | W_d row]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + static_cast<size_t>(P) * 2 * row_bytes);
+  Entry* list = reinterpret_cast<Entry*>(bars + kMaxStages);
+
+  if (lane == 0) {
+    for (int s = 0; s < P; ++s) ptx::mbar_init(&bars[s], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto own = [&](int i) { return EXACT || (lane + 32 * i) < nch; };
+  uint32_t seq = 0;  // entries issued (and consumed) so far by this warp
+
+  auto issue = [&](const Entry& e, uint32_t n) {
+    const int s = static_cast<int>(n % static_cast<uint32_t>(P));
+    uint8_t* dst = stages + static_cast<size_t>(s) * 2 * row_bytes;
+    ptx::mbar_arrive_expect_tx(&bars[s], 2 * row_bytes);
+    ptx::bulk_load(dst, p.Wu_t + static_cast<size_t>(e.j) * D, row_bytes, &bars[s]);
+    ptx::bulk_load(dst + row_bytes, p.Wd + static_cast<size_t>(e.j) * D, row_bytes, &bars[s]);
+  };
+
+  const int warps_total = gridDim.x * kWarps;
+  const long long units = static_cast<long long>(p.T) * p.upr;
+  for (long long u = static_cast<long long>(blockIdx.x) * kWarps + wid; u < units;
+       u += warps_total) {
+    const int t = static_cast<int>(u / p.upr);
+    const int k_begin = static_cast<int>(u % p.upr) * p.G;
+    const int k_end = min(k_begin + p.G, p.n_t);
+    float xf[NC][8];
+    float acc[NC][8];
+    bool have_x = false;
+    bool any = false;
+    const uint16_t* xr = p.x + static_cast<size_t>(t) * D;
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
-      uint4 v = st.own(i, lane, nch) ? ldg16(xr + 8 * (lane + 32 * i)) : make_uint4(0, 0, 0, 0);
-      st.x[i][0] = v.x;
-      st.x[i][1] = v.y;
-      st.x[i][2] = v.z;
-      st.x[i][3] = v.w;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) st.acc[i][e] = 0.0f;
+      for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
     }
 
     const size_t row_rt = static_cast<size_t>(t) * p.n_t;
-    for (int kb = 0; kb < p.n_t; kb += 32) {
+    for (int kb = k_begin; kb < k_end; kb += 32) {
       const int k = kb + lane;
-      const int c = k < p.n_t ? p.cnt[row_rt + k] : 0;
-      uint32_t m = __ballot_sync(0xffffffffu, c > 0);
-      while (m) {
-        const int src = __ffs(m) - 1;
-        m &= m - 1;
-        const int kt = kb + src;
-        const int cc = __shfl_sync(0xffffffffu, c, src);
-        const size_t rt = row_rt + kt;
-        if (cc <= p.W) {
-          // slots: lane s holds slot s of this (row, tile)
-          for (int s0 = 0; s0 < cc; s0 += 32) {
-            const int s = s0 + lane;
-            int jl = 0;
-            float hl = 0.0f;
-            if (s < cc) {
-              jl = p.col[rt * p.W + s];
-              hl = p.val[rt * p.W + s];
-            }
-            const int n = min(32, cc - s0);
-            for (int qq = 0; qq < n; ++qq) {
-              const int j = kt * TWELL_TILE + __shfl_sync(0xffffffffu, jl, qq);
-              const float h = __shfl_sync(0xffffffffu, hl, qq);
-              st.nonzero(p, j, h, lane, nch);
-            }
-          }
-        } else {
-          const int slot = p.spill_slot[rt];
-          if (slot < 0 || slot >= p.spill_cap) {
-            if (lane == 0 && p.status) atomicOr(p.status, TWELL_FLAG_SPILL_FULL);
-            continue;
-          }
-          const float* sl = p.spill_val + static_cast<size_t>(slot) * TWELL_TILE;
-#pragma unroll 1
-          for (int g = 0; g < TWELL_TILE / 32; ++g) {
-            const float hv = sl[g * 32 + lane];
-            // stored values are ReLU outputs: positive means active
-            uint32_t mm = __ballot_sync(0xffffffffu, hv > 0.0f);
-            while (mm) {
-              const int qq = __ffs(mm) - 1;
-              mm &= mm - 1;
-              const float h = __shfl_sync(0xffffffffu, hv, qq);
-              st.nonzero(p, kt * TWELL_TILE + g * 32 + qq, h, lane, nch);
-            }
+      const int c = k < k_end ? p.cnt[row_rt + k] : 0;
+      // entries of tile k: its slots, or the positives of its spill slice
+      // (the spill holds exactly c positive values)
+      int spill = -1;
+      if (c > p.W) {
+        spill = p.spill_slot[row_rt + k];
+        if (spill < 0 || spill >= p.spill_cap) {
+          atomicOr(p.status, TWELL_FLAG_SPILL_FULL);
+          spill = -2;
+        }
+      }
+      const int n = spill == -2 ? 0 : c;
+      int off = n;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, off, d);
+        if (lane >= d) off += v;
+      }
+      const int total = __shfl_sync(0xffffffffu, off, 31);
+      off -= n;
+      if (total > 0 && !have_x) {
+        have_x = true;
+        any = true;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+          uint4 v = own(i) ? __ldg(reinterpret_cast<const uint4*>(xr + 8 * (lane + 32 * i)))
+                           : make_uint4(0, 0, 0, 0);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            xf[i][2 * e] = bf16lo(w4[e]);
+            xf[i][2 * e + 1] = bf16hi(w4[e]);
           }
         }
       }
+
+      for (int base = 0; base < total; base += kListCap) {
+        // list the entries whose position falls in [base, base + kListCap)
+        if (n > 0 && off + n > base && off < base + kListCap) {
+          const int jbase = k * TWELL_TILE;
+          if (spill < 0) {
+            const size_t so = (row_rt + k) * static_cast<size_t>(p.W);
+            const int s0 = max(0, base - off);
+            const int s1 = min(n, base + kListCap - off);
+            for (int s = s0; s < s1; ++s)
+              list[off + s - base] = Entry{jbase + p.col[so + s], p.val[so + s]};
+          } else {
+            const float* sl = p.spill_val + static_cast<size_t>(spill) * TWELL_TILE;
+            int e = off;
+            for (int cc = 0; cc < TWELL_TILE && e < base + kListCap; ++cc) {
+              const float v = sl[cc];
+              if (v > 0.0f) {
+                if (e >= base) list[e - base] = Entry{jbase + cc, v};
+                ++e;
+              }
+            }
+          }
+        }
+        __syncwarp();
+        const int m = min(kListCap, total - base);
+        if (lane == 0) {
+          const int pre = min(P, m);
+          for (int i = 0; i < pre; ++i) issue(list[i], seq + i);
+        }
+        for (int i = 0; i < m; ++i) {
+          const uint32_t n_i = seq + i;
+          const int s = static_cast<int>(n_i % static_cast<uint32_t>(P));
+          // warp-uniform decision: the lanes shuffle together below
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars[s], (n_i / P) & 1u))) {
+            if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            return;
+          }
+          const Entry e = list[i];
+          const uint4* su =
+              reinterpret_cast<const uint4*>(stages + static_cast<size_t>(s) * 2 * row_bytes);
+          const uint4* sd = su + nch;
+          float pp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int q = 0; q < NC; ++q) {
+            if (own(q)) {
+              const uint4 a = su[lane + 32 * q];
+              const uint32_t a4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                pp[r] = fmaf(xf[q][2 * r], bf16lo(a4[r]), pp[r]);
+                pp[r] = fmaf(xf[q][2 * r + 1], bf16hi(a4[r]), pp[r]);
+              }
+            }
+          }
+          float part = (pp[0] + pp[1]) + (pp[2] + pp[3]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          const float sc = e.h * part;
+#pragma unroll
+          for (int q = 0; q < NC; ++q) {
+            if (own(q)) {
+              const uint4 b = sd[lane + 32 * q];
+              const uint32_t b4[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                acc[q][2 * r] = fmaf(sc, bf16lo(b4[r]), acc[q][2 * r]);
+                acc[q][2 * r + 1] = fmaf(sc, bf16hi(b4[r]), acc[q][2 * r + 1]);
+              }
+            }
+          }
+          // every lane is done reading stage s before it is refilled
+          __syncwarp();
+          if (lane == 0 && i + P < m) {
+            ptx::fence_proxy_async_smem();
+            issue(list[i + P], n_i + P);
+          }
+        }
+        seq += static_cast<uint32_t>(m);
+        __syncwarp();  // the list is rewritten by the next pass
+      }
     }
 
-    float* yr = p.y + static_cast<size_t>(t) * p.D;
+    float* yr = p.y + static_cast<size_t>(t) * D;
+    if (p.split) {
+      if (any) {
 #pragma unroll
-    for (int i = 0; i < NC; ++i) {
-      if (st.own(i, lane, nch)) {
-        float4* o = reinterpret_cast<float4*>(yr + 8 * (lane + 32 * i));
-        o[0] = make_float4(st.acc[i][0], st.acc[i][1], st.acc[i][2], st.acc[i][3]);
-        o[1] = make_float4(st.acc[i][4], st.acc[i][5], st.acc[i][6], st.acc[i][7]);
+        for (int i = 0; i < NC; ++i) {
+          if (own(i)) {
+            float4* o = reinterpret_cast<float4*>(yr + 8 * (lane + 32 * i));
+            atomicAdd(o, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+            atomicAdd(o + 1, make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
+        if (own(i)) {
+          float4* o = reinterpret_cast<float4*>(yr + 8 * (lane + 32 * i));
+          o[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+          o[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+        }
       }
     }
   }
 }
 
 template <int NC>
-twell_status launch_nc(const FfnParams& p, const DeviceInfo& dev, cudaStream_t s) {
+twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
+  const int stage_bytes = 4 * p.D;
+  const int fixed = kMaxStages * 8 + kListCap * static_cast<int>(sizeof(Entry));
+  int P = (kSmemBudget / kWarps - fixed) / stage_bytes;
+  if (P > kMaxStages) P = kMaxStages;
+  if (P < 1) return TWELL_ERR_UNSUPPORTED;
+  p.stages = P;
+  p.warp_bytes = (P * stage_bytes + fixed + 15) & ~15;
+  const int smem = kWarps * p.warp_bytes;
   const bool exact = p.D == 256 * NC;
-  const int threads = 256;
-  const long long want = (static_cast<long long>(p.T) * 32 + threads - 1) / threads;
-  const int grid = static_cast<int>(want < 65535LL * 8 ? want : 65535LL * 8);
-  (void)dev;
-  if (exact)
-    ffn_fwd_kernel<NC, true><<<grid, threads, 0, s>>>(p);
-  else
-    ffn_fwd_kernel<NC, false><<<grid, threads, 0, s>>>(p);
+  auto kern = exact ? ffn_fwd_kernel<NC, true> : ffn_fwd_kernel<NC, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return TWELL_ERR_CUDA;
+  // Whole rows per unit when there are enough rows to fill every warp a few
+  // times over; otherwise split rows into tile ranges (atomics into y).
+  const long long warps_total = static_cast<long long>(dev.sm_count) * kWarps;
+  if (p.T >= 4 * warps_total) {
+    p.G = p.n_t;
+  } else {
+    long long g = static_cast<long long>(p.n_t) * p.T / (4 * warps_total);
+    p.G = static_cast<int>(g < 1 ? 1 : (g > p.n_t ? p.n_t : g));
+  }
+  p.upr = (p.n_t + p.G - 1) / p.G;
+  p.split = p.upr > 1;
+  if (p.split &&
+      cudaMemsetAsync(p.y, 0, static_cast<size_t>(p.T) * p.D * sizeof(float), s) != cudaSuccess)
+    return TWELL_ERR_CUDA;
+  const long long units = static_cast<long long>(p.T) * p.upr;
+  const long long want = (units + kWarps - 1) / kWarps;
+  const int grid = static_cast<int>(want < dev.sm_count ? want : dev.sm_count);
+  kern<<<grid, kWarps * 32, smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
@@ -199,7 +306,7 @@ extern "C" twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const
   twell_status st = check_twell(h, T, F, false);
   if (st != TWELL_OK) return st;
   if (T == 0) return TWELL_OK;
-  if (!x || !Wu_t || !Wd || !y) return TWELL_ERR_INVALID;
+  if (!x || !Wu_t || !Wd || !y || !status_dev) return TWELL_ERR_INVALID;
   if (!aligned16(x) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y))
     return TWELL_ERR_INVALID;
   if (D > 256 * 12) return TWELL_ERR_UNSUPPORTED;

@@ -192,13 +192,20 @@ def run_ours(args, w):
     x, Wg, Wu, Wd = up(w.x), up(w.Wg_t), up(w.Wu_t), up(w.Wd)
     h = tw.TwELL(w.T, w.F, w.width, device=dev)
     y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = torch.empty((0 if args.no_flush else 512) * 1024 * 1024, dtype=torch.uint8,
+                        device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         tw.twell_gate_pack(x, Wg, h, stream=stream)
         tw.twell_ffn_fwd(x, h, Wu, Wd, y=y, stream=stream)
 
+    # active-neuron union (for the fused kernel's algorithmic bytes), from
+    # one untimed pack with the gate pre-activations exported
+    zdbg = torch.empty((w.T, w.F), dtype=torch.float32, device=dev)
+    tw.twell_gate_pack(x, Wg, h, z_debug=zdbg, stream=stream)
+    n_active = int((zdbg > 0).any(dim=0).sum().item())
+    del zdbg
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -259,9 +266,9 @@ def run_ours(args, w):
     k1_flops = 2.0 * w.T * w.D * w.F
     k1_tf = k1_flops / (k1_ms * 1e-3) / 1e12
     # fused kernel: algorithmic bytes = x in (bf16) + y out (fp32) + W_u/W_d
-    # rows of every neuron (all are active in some row at these sizes) + the
-    # TwELL entries read (5 B per nnz: fp32 value + u8 column, 1 B per count)
-    k2_bytes = w.T * w.D * (2 + 4) + w.F * w.D * 2 * 2 + 5 * nnz + w.T * (w.F // 128)
+    # rows of every neuron active in some row + the TwELL entries read (5 B
+    # per nnz: fp32 value + u8 column, 1 B per count)
+    k2_bytes = w.T * w.D * (2 + 4) + n_active * w.D * 2 * 2 + 5 * nnz + w.T * (w.F // 128)
     k2_gbs = k2_bytes / (k2_ms * 1e-3) / 1e9
     kernels = {
         "twell_gate_pack": {"ms": k1_ms, "tflops": k1_tf, "frac_bf16": k1_tf / bf16},
@@ -282,8 +289,10 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F,
-                   "twell_width": w.width, "nnz": nnz,
-                   "density": nnz / (w.T * w.F), "l2": "flushed (512 MiB write) before every step",
+                   "twell_width": w.width, "nnz": nnz, "active_neurons": n_active,
+                   "density": nnz / (w.T * w.F),
+                   "l2": ("NOT flushed (profiling run)" if args.no_flush
+                          else "flushed (512 MiB write) before every step"),
                    "parallelism": f"replicas x{ws}"},
         "e2e": {"value": ws * w.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -311,11 +320,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--T", type=int, default=None, help="token count override")
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true",
+                    help="skip the L2 flush (profiling runs only; not a valid bench number)")
     args = ap.parse_args()
     import workloads
-    w = workloads.config(args.config)
+    w = workloads.config(args.config, T=args.T)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

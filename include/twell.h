@@ -129,7 +129,10 @@ twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T,
  *   y   [T][D] fp32 (written; fp32 because a bf16 output alone can exceed a
  *       2e-2 * RMS(y) error where |y| reaches 10 * RMS)
  * A (row, tile) whose spill slice is missing (index >= spill_cap) is skipped
- * and TWELL_FLAG_SPILL_FULL is set.
+ * and TWELL_FLAG_SPILL_FULL is set.  With few rows (decode batches) a row is
+ * split over several warps whose partial sums are added with float atomics
+ * into y (zeroed first), so repeated calls agree to fp32 rounding, not bit
+ * for bit; with many rows each row is summed by one warp in a fixed order.
  */
 twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
                            const uint16_t* Wd, int32_t D, float* y, int32_t* status_dev,

@@ -128,7 +128,9 @@ def test_side_stream_and_repeat():
         tw.twell_gate_pack(d["x"], d["Wg_t"], h, stream=s)
         y2 = tw.twell_ffn_fwd(d["x"], h, d["Wu_t"], d["Wd"], stream=s)
     s.synchronize()
-    assert torch.equal(y1, y2)
+    # rows split over several warps (few tokens) accumulate with float
+    # atomics, so repeats agree to fp32 rounding rather than bit for bit
+    torch.testing.assert_close(y1, y2, rtol=1e-5, atol=1e-6)
     check_y(y2.cpu().numpy().astype(np.float64), w, tw_z(w, d))
 
 
