@@ -17,7 +17,9 @@ import os
 import torch
 
 __all__ = [
-    "TwellError", "TwELL", "lib", "twell_gate_pack", "twell_ffn_fwd", "twell_status_string",
+    "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
+    "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_bwd",
+    "twell_status_string",
     "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "TILE",
 ]
 
@@ -41,6 +43,16 @@ class TwellStruct(ctypes.Structure):
     ]
 
 
+class HybridStruct(ctypes.Structure):
+    """Mirror of ``hybrid_t``."""
+    _fields_ = [
+        ("T", c_i32), ("F", c_i32), ("tile", c_i32), ("cap", c_i32), ("max_dense", c_i32),
+        ("n_ell", c_ptr), ("n_dense", c_ptr), ("row_map", c_ptr), ("ell_rows", c_ptr),
+        ("ell_val", c_ptr), ("ell_col", c_ptr), ("ell_cnt", c_ptr), ("dense_rows", c_ptr),
+        ("dense_h", c_ptr),
+    ]
+
+
 class TwellError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
@@ -55,6 +67,14 @@ _SIGNATURES = {
                                 c_ptr, c_ptr, c_ptr]),
     "twell_ffn_fwd": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
                               c_ptr, c_ptr]),
+    "twell_to_hybrid": (c_i32, [ctypes.POINTER(TwellStruct), ctypes.POINTER(HybridStruct),
+                                c_ptr, c_ptr]),
+    "twell_workspace_size": (ctypes.c_size_t, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "hybrid_ffn_fwd": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_i32, c_ptr,
+                               c_ptr, c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "hybrid_ffn_bwd": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_ptr, c_ptr,
+                               c_ptr, c_i32, c_ptr, ctypes.c_float, c_ptr, c_ptr, c_ptr, c_ptr,
+                               c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "twell_status_string": (ctypes.c_char_p, [c_i32]),
     "twell_version": (c_i32, []),
 }
@@ -174,3 +194,117 @@ def twell_ffn_fwd(x, h: TwELL, Wu_t, Wd, y=None, status=None, stream=None):
                                    _ptr(y), _ptr(status), _stream(stream)),
                "twell_ffn_fwd")
     return y
+
+
+class Hybrid:
+    """Device buffers of the hybrid training format (ELL rows + dense
+    backup) and the ``hybrid_t`` descriptor pointing at them."""
+
+    def __init__(self, T: int, F: int, cap: int, max_dense: int, device=None,
+                 tile: int = TILE):
+        device = torch.device(device if device is not None else "cuda")
+        n_t = F // tile
+        self.T, self.F, self.cap, self.max_dense, self.tile, self.n_t = (
+            T, F, cap, max_dense, tile, n_t)
+        self.device = device
+        i32 = torch.int32
+        self.counts = torch.zeros((2,), dtype=i32, device=device)  # n_ell, n_dense
+        self.row_map = torch.empty((max(T, 1),), dtype=i32, device=device)
+        self.ell_rows = torch.empty((max(T, 1),), dtype=i32, device=device)
+        self.ell_val = torch.empty((T, n_t, cap), dtype=torch.float32, device=device)
+        self.ell_col = torch.empty((T, n_t, cap), dtype=torch.uint8, device=device)
+        self.ell_cnt = torch.empty((T, n_t), dtype=torch.uint8, device=device)
+        self.dense_rows = torch.empty((max(max_dense, 1),), dtype=i32, device=device)
+        self.dense_h = torch.empty((max(max_dense, 1), F), dtype=torch.float32, device=device)
+        self.status = torch.zeros((1,), dtype=i32, device=device)
+        base = self.counts.data_ptr()
+        self.struct = HybridStruct(
+            T, F, tile, cap, max_dense, base, base + 4, self.row_map.data_ptr(),
+            self.ell_rows.data_ptr(), self.ell_val.data_ptr(), self.ell_col.data_ptr(),
+            self.ell_cnt.data_ptr(), self.dense_rows.data_ptr(), self.dense_h.data_ptr())
+
+    @property
+    def n_ell(self) -> int:
+        return int(self.counts[0].item())
+
+    @property
+    def n_dense(self) -> int:
+        return int(self.counts[1].item())
+
+
+def twell_to_hybrid(h: TwELL, out: Hybrid, status=None, stream=None):
+    """TwELL -> hybrid (ELL rows with capacity out.cap, dense backup)."""
+    if out.T != h.T or out.F != h.F:
+        raise ValueError("hybrid and TwELL shapes differ")
+    status = out.status if status is None else status
+    with torch.cuda.device(out.device):
+        _check(lib().twell_to_hybrid(ctypes.byref(h.struct), ctypes.byref(out.struct),
+                                     _ptr(status), _stream(stream)), "twell_to_hybrid")
+    return out
+
+
+WS_HYBRID_FWD = 1
+WS_HYBRID_BWD = 2
+
+
+def twell_workspace_size(op: int, T: int, D: int, F: int, cap: int, max_dense: int) -> int:
+    return int(lib().twell_workspace_size(op, T, D, F, cap, max_dense))
+
+
+def _workspace(nbytes, device):
+    # 256-byte aligned scratch from torch's allocator (its blocks are 512-aligned)
+    return torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=device)
+
+
+def hybrid_ffn_fwd(x, h: Hybrid, Wu_t, Wd, y=None, u_ell=None, U_dense=None, ws=None,
+                   status=None, stream=None):
+    """Hybrid training forward; returns (y, u_ell, U_dense)."""
+    _need(x, torch.bfloat16, "x")
+    _need(Wu_t, torch.bfloat16, "Wu_t")
+    _need(Wd, torch.bfloat16, "Wd")
+    T, D = x.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    if u_ell is None:
+        u_ell = torch.empty((T, h.n_t, h.cap), dtype=torch.float32, device=dev)
+    if U_dense is None:
+        U_dense = torch.empty((max(h.max_dense, 1), h.F), dtype=torch.float32, device=dev)
+    need = twell_workspace_size(WS_HYBRID_FWD, T, D, h.F, h.cap, h.max_dense)
+    if ws is None:
+        ws = _workspace(need, dev)
+    status = h.status if status is None else status
+    with torch.cuda.device(dev):
+        _check(lib().hybrid_ffn_fwd(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
+                                    _ptr(y), _ptr(u_ell), _ptr(U_dense), _ptr(ws),
+                                    ws.numel(), _ptr(status), _stream(stream)),
+               "hybrid_ffn_fwd")
+    return y, u_ell, U_dense
+
+
+def hybrid_ffn_bwd(x, h: Hybrid, u_ell, U_dense, Wg_t, Wu_t, Wd, dy, l1_coeff, dx=None,
+                   dWg_t=None, dWu_t=None, dWd=None, ws=None, status=None, stream=None):
+    """Hybrid training backward with the L1 term; returns (dx, dWg_t, dWu_t, dWd)."""
+    for t, n in ((x, "x"), (Wg_t, "Wg_t"), (Wu_t, "Wu_t"), (Wd, "Wd")):
+        _need(t, torch.bfloat16, n)
+    _need(dy, torch.float32, "dy")
+    T, D = x.shape
+    F = h.F
+    dev = x.device
+    f32 = torch.float32
+    dx = torch.empty((T, D), dtype=f32, device=dev) if dx is None else dx
+    dWg_t = torch.empty((F, D), dtype=f32, device=dev) if dWg_t is None else dWg_t
+    dWu_t = torch.empty((F, D), dtype=f32, device=dev) if dWu_t is None else dWu_t
+    dWd = torch.empty((F, D), dtype=f32, device=dev) if dWd is None else dWd
+    need = twell_workspace_size(WS_HYBRID_BWD, T, D, F, h.cap, h.max_dense)
+    if ws is None:
+        ws = _workspace(need, dev)
+    status = h.status if status is None else status
+    with torch.cuda.device(dev):
+        _check(lib().hybrid_ffn_bwd(_ptr(x), ctypes.byref(h.struct), _ptr(u_ell), _ptr(U_dense),
+                                    _ptr(Wg_t), _ptr(Wu_t), _ptr(Wd), D, _ptr(dy),
+                                    float(l1_coeff), _ptr(dx), _ptr(dWg_t), _ptr(dWu_t),
+                                    _ptr(dWd), _ptr(ws), ws.numel(), _ptr(status),
+                                    _stream(stream)),
+               "hybrid_ffn_bwd")
+    return dx, dWg_t, dWu_t, dWd

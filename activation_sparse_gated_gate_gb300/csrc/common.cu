@@ -65,7 +65,8 @@ twell_status check_twell(const twell_t* h, int32_t T, int32_t F, bool need_spill
 }
 
 twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
-                               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+                               uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                               uint64_t pitch) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -76,7 +77,7 @@ twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
   });
   if (!g_encode) return TWELL_ERR_CUDA;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {(pitch ? pitch : inner) * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,

@@ -31,9 +31,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Validate a TwELL descriptor against the expected T and F.
 twell_status check_twell(const twell_t* h, int32_t T, int32_t F, bool need_spill_n);
 
-// 2-D bf16 tensor map over a row-major [outer][inner] array, box
-// [box_outer][box_inner], 128-byte swizzle, zero fill out of bounds.
+// Validate a hybrid descriptor against the expected T and F.
+twell_status check_hybrid(const hybrid_t* h, int32_t T, int32_t F);
+
+// 2-D bf16 tensor map over a row-major [outer][inner] array whose rows are
+// `pitch` elements apart (pitch = inner when 0), box [box_outer][box_inner],
+// 128-byte swizzle, zero fill out of bounds.
 twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
-                               uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+                               uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                               uint64_t pitch = 0);
 
 }  // namespace twell

@@ -21,7 +21,7 @@
 // staged rows with 16-byte shared loads, form u = x_t . W_u[:, j] with four
 // independent partial sums and a butterfly reduction, and accumulate
 // (h u) W_d[j, :].
-#include "common.cuh"
+#include "fused.cuh"
 #include "ptx.cuh"
 
 namespace twell {
@@ -32,37 +32,12 @@ constexpr int kListCap = 256;        // entries listed per pass
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 220 * 1024;
 
-struct FfnParams {
-  const uint16_t* x;
-  const uint16_t* Wu_t;
-  const uint16_t* Wd;
-  float* y;
-  const float* val;
-  const uint8_t* col;
-  const uint8_t* cnt;
-  const int32_t* spill_slot;
-  const float* spill_val;
-  int32_t spill_cap;
-  int32_t T, D, n_t, W;
-  int32_t G;           // column tiles per work unit
-  int32_t upr;         // units per token row, ceil(n_t / G)
-  int32_t split;       // rows split over several units: accumulate with atomics
-  int32_t stages;      // P
-  int32_t warp_bytes;  // shared memory per warp
-  int32_t* status;
-};
-
-struct Entry {
-  int32_t j;
-  float h;
-};
-
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // NC = 8-element chunks per lane (D <= 256 * NC).  EXACT: D == 256 * NC, so
 // every lane owns all NC of its chunks.
-template <int NC, bool EXACT>
+template <int NC, bool EXACT, bool ELL>
 __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -95,10 +70,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
   };
 
   const int warps_total = gridDim.x * kWarps;
-  const long long units = static_cast<long long>(p.T) * p.upr;
+  const long long units =
+      ELL ? static_cast<long long>(*p.n_rows) : static_cast<long long>(p.T) * p.upr;
   for (long long u = static_cast<long long>(blockIdx.x) * kWarps + wid; u < units;
        u += warps_total) {
-    const int t = static_cast<int>(u / p.upr);
+    // row: index into the count / slot arrays; t: token (x and y row)
+    const int row = ELL ? static_cast<int>(u) : static_cast<int>(u / p.upr);
+    const int t = ELL ? p.ell_rows[row] : row;
     const int k_begin = static_cast<int>(u % p.upr) * p.G;
     const int k_end = min(k_begin + p.G, p.n_t);
     float xf[NC][8];
@@ -112,14 +90,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
       for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
     }
 
-    const size_t row_rt = static_cast<size_t>(t) * p.n_t;
+    const size_t row_rt = static_cast<size_t>(row) * p.n_t;
     for (int kb = k_begin; kb < k_end; kb += 32) {
       const int k = kb + lane;
       const int c = k < k_end ? p.cnt[row_rt + k] : 0;
       // entries of tile k: its slots, or the positives of its spill slice
       // (the spill holds exactly c positive values)
       int spill = -1;
-      if (c > p.W) {
+      if (!ELL && c > p.W) {
         spill = p.spill_slot[row_rt + k];
         if (spill < 0 || spill >= p.spill_cap) {
           atomicOr(p.status, TWELL_FLAG_SPILL_FULL);
@@ -160,14 +138,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
             const int s0 = max(0, base - off);
             const int s1 = min(n, base + kListCap - off);
             for (int s = s0; s < s1; ++s)
-              list[off + s - base] = Entry{jbase + p.col[so + s], p.val[so + s]};
+              list[off + s - base] =
+                  Entry{jbase + p.col[so + s], p.val[so + s], static_cast<int32_t>(so + s)};
           } else {
             const float* sl = p.spill_val + static_cast<size_t>(spill) * TWELL_TILE;
             int e = off;
             for (int cc = 0; cc < TWELL_TILE && e < base + kListCap; ++cc) {
               const float v = sl[cc];
               if (v > 0.0f) {
-                if (e >= base) list[e - base] = Entry{jbase + cc, v};
+                if (e >= base) list[e - base] = Entry{jbase + cc, v, 0};
                 ++e;
               }
             }
@@ -207,6 +186,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
           float part = (pp[0] + pp[1]) + (pp[2] + pp[3]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          if (ELL && lane == 0) p.u_save[e.pos] = part;
           const float sc = e.h * part;
 #pragma unroll
           for (int q = 0; q < NC; ++q) {
@@ -257,7 +237,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
   }
 }
 
-template <int NC>
+template <int NC, bool ELL>
 twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
   const int stage_bytes = 4 * p.D;
   const int fixed = kMaxStages * 8 + kListCap * static_cast<int>(sizeof(Entry));
@@ -268,14 +248,14 @@ twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
   p.warp_bytes = (P * stage_bytes + fixed + 15) & ~15;
   const int smem = kWarps * p.warp_bytes;
   const bool exact = p.D == 256 * NC;
-  auto kern = exact ? ffn_fwd_kernel<NC, true> : ffn_fwd_kernel<NC, false>;
+  auto kern = exact ? ffn_fwd_kernel<NC, true, ELL> : ffn_fwd_kernel<NC, false, ELL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return TWELL_ERR_CUDA;
   // Whole rows per unit when there are enough rows to fill every warp a few
   // times over; otherwise split rows into tile ranges (atomics into y).
   const long long warps_total = static_cast<long long>(dev.sm_count) * kWarps;
-  if (p.T >= 4 * warps_total) {
+  if (ELL || p.T >= 4 * warps_total) {
     p.G = p.n_t;
   } else {
     long long g = static_cast<long long>(p.n_t) * p.T / (4 * warps_total);
@@ -294,6 +274,30 @@ twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
 }
 
 }  // namespace
+
+twell_status launch_fused(const FfnParams& p, const DeviceInfo& dev, cudaStream_t s, bool ell) {
+#define TWELL_NC_CASE(n) \
+  case n:                \
+    return ell ? launch_nc<n, true>(p, dev, s) : launch_nc<n, false>(p, dev, s);
+  switch ((p.D + 255) / 256) {
+    TWELL_NC_CASE(1)
+    TWELL_NC_CASE(2)
+    TWELL_NC_CASE(3)
+    TWELL_NC_CASE(4)
+    TWELL_NC_CASE(5)
+    TWELL_NC_CASE(6)
+    TWELL_NC_CASE(7)
+    TWELL_NC_CASE(8)
+    TWELL_NC_CASE(9)
+    TWELL_NC_CASE(10)
+    TWELL_NC_CASE(11)
+    TWELL_NC_CASE(12)
+    default:
+      return TWELL_ERR_UNSUPPORTED;
+  }
+#undef TWELL_NC_CASE
+}
+
 }  // namespace twell
 
 extern "C" twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
@@ -329,20 +333,8 @@ extern "C" twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const
   p.n_t = F / TWELL_TILE;
   p.W = h->width;
   p.status = status_dev;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  switch ((D + 255) / 256) {
-    case 1: return launch_nc<1>(p, dev, s);
-    case 2: return launch_nc<2>(p, dev, s);
-    case 3: return launch_nc<3>(p, dev, s);
-    case 4: return launch_nc<4>(p, dev, s);
-    case 5: return launch_nc<5>(p, dev, s);
-    case 6: return launch_nc<6>(p, dev, s);
-    case 7: return launch_nc<7>(p, dev, s);
-    case 8: return launch_nc<8>(p, dev, s);
-    case 9: return launch_nc<9>(p, dev, s);
-    case 10: return launch_nc<10>(p, dev, s);
-    case 11: return launch_nc<11>(p, dev, s);
-    case 12: return launch_nc<12>(p, dev, s);
-    default: return TWELL_ERR_UNSUPPORTED;
-  }
+  p.n_rows = nullptr;
+  p.ell_rows = nullptr;
+  p.u_save = nullptr;
+  return launch_fused(p, dev, static_cast<cudaStream_t>(stream), false);
 }

@@ -1,0 +1,505 @@
+// tcgen05 GEMM for the dense-overflow rows of the hybrid training format
+// ("Sparser, Faster, Lighter Transformer Language Models", section 2.B.3:
+// overflow rows are routed to a dense backup, whose contractions run here on
+// the tensor cores), plus the transpose / gather kernels preparing its
+// operands.
+//
+// C[M][N] = sum over K segments of A_s[M][K_s] * B_s[N][K_s]^T, bf16 inputs,
+// fp32 accumulation in TMEM.  Same warp layout as the gate kernel: a TMA
+// producer warp, an MMA-issuing warp, four epilogue warps, two TMEM
+// accumulator buffers, persistent CTAs.  K segments let one accumulator sum
+// the bf16 hi and lo halves of an fp32 operand (v = hi + lo with |lo| <=
+// 2^-9 |v|, so hi*B + lo*B carries v*B with a relative error near 2^-17);
+// the row count may be a device value (number of overflow rows), in which
+// case row tiles past it are skipped by every role.
+#include <cuda_bf16.h>
+
+#include "gemm.cuh"
+#include "ptx.cuh"
+
+namespace twell {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 256 + 1024;
+};
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float bf16_val(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ void split(float v, uint16_t& hi, uint16_t& lo) {
+  hi = bf16_bits(v);
+  lo = bf16_bits(v - bf16_val(hi));
+}
+
+// Epilogue of one 32-column chunk of tile row m (global), columns
+// n0 .. n0+31; `full` when all 32 columns are inside N.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int m, int n0,
+                                               const uint32_t (&r)[32], bool full) {
+  const int N = p.N;
+  if ((EPI == EPI_STORE || EPI == EPI_ADD) && p.ksplit > 1) {
+    const int64_t row = p.row_idx ? p.row_idx[m] : m;
+    float* c = p.C + row * p.ldc + n0;
+    if (full) {
+      float4* c4 = reinterpret_cast<float4*>(c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        atomicAdd(c4 + i, make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                      __uint_as_float(r[4 * i + 2]),
+                                      __uint_as_float(r[4 * i + 3])));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < N) atomicAdd(c + i, __uint_as_float(r[i]));
+    }
+  } else if (EPI == EPI_STORE || EPI == EPI_ADD) {
+    const int64_t row = p.row_idx ? p.row_idx[m] : m;
+    float* c = p.C + row * p.ldc + n0;
+    if (full) {
+      float4* c4 = reinterpret_cast<float4*>(c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                               __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        if (EPI == EPI_ADD) {
+          const float4 o = c4[i];
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        c4[i] = v;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (n0 + i < N) {
+          const float v = __uint_as_float(r[i]);
+          c[i] = EPI == EPI_ADD ? c[i] + v : v;
+        }
+      }
+    }
+  } else if (EPI == EPI_UP) {
+    const int64_t off = static_cast<int64_t>(m) * N + n0;
+    const float* h = p.H + off;
+    float* uo = p.U_out + off;
+    uint16_t* hi = p.S_out + static_cast<int64_t>(m) * p.lds + n0;
+    uint16_t* lo = hi + N;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (full || n0 + i < N) {
+        const float u = __uint_as_float(r[i]);
+        uo[i] = u;
+        uint16_t a_hi, a_lo;
+        split(h[i] * u, a_hi, a_lo);
+        hi[i] = a_hi;
+        lo[i] = a_lo;
+      }
+    }
+  } else {  // EPI_DA
+    const int64_t off = static_cast<int64_t>(m) * N + n0;
+    const float* h = p.H + off;
+    const float* u = p.U_in + off;
+    uint16_t* s = p.S_out + static_cast<int64_t>(m) * p.lds + n0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (full || n0 + i < N) {
+        const float da = __uint_as_float(r[i]);
+        const float hv = h[i];
+        const float dz = hv > 0.0f ? fmaf(da, u[i], p.lambda) : 0.0f;
+        const float du = da * hv;
+        uint16_t a, b;
+        split(dz, a, b);
+        s[i] = a;
+        s[i + N] = b;
+        split(du, a, b);
+        s[i + 2 * N] = a;
+        s[i + 3 * N] = b;
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs p, int num_m, int num_n) {
+  using C = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // extents known only on the device (rows and K lengths of this call)
+  const int M_act = p.M_dyn ? min(p.M, *p.M_dyn) : p.M;
+  int kb_seg[kGemmMaxSeg];
+  int total_kb = 0;
+#pragma unroll
+  for (int s = 0; s < kGemmMaxSeg; ++s) {
+    int len = 0;
+    if (s < p.nseg) {
+      len = p.seg[s].len;
+      if (p.seg[s].len_dyn) len = min(len, *p.seg[s].len_dyn);
+    }
+    kb_seg[s] = len > 0 ? (len + BK - 1) / BK : 0;
+    total_kb += kb_seg[s];
+  }
+  const int num_tiles = num_m * num_n;
+  const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
+  const int num_units = num_tiles * ksplit;
+  const int kb_chunk = (total_kb + ksplit - 1) / ksplit;
+  // unit -> (tile, k-block range); every role skips the same units
+  auto unit_range = [&](int u, int& m_blk, int& n_blk, int& kb0, int& kb1) {
+    const int tile = u % num_tiles;
+    const int ks = u / num_tiles;
+    m_blk = tile % num_m;
+    n_blk = tile / num_m;
+    kb0 = ks * kb_chunk;
+    kb1 = min(total_kb, kb0 + kb_chunk);
+    return m_blk * BM < M_act && kb0 < kb1;
+  };
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kGemmMaxSeg; ++s) {
+      if (s < p.nseg) {
+        ptx::prefetch_tmap(&maps.a[p.seg[s].map_a]);
+        ptx::prefetch_tmap(&maps.b[p.seg[s].map_b]);
+      }
+    }
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 128);
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (total_kb > 0) {
+    if (warp == 0) {
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+          int m_blk, n_blk, kb0, kb1;
+          if (!unit_range(u, m_blk, n_blk, kb0, kb1)) continue;
+          int seg_first = 0;  // global index of the segment's first k block
+          for (int s = 0; s < p.nseg; seg_first += kb_seg[s], ++s) {
+            const CUtensorMap* ma = &maps.a[p.seg[s].map_a];
+            const CUtensorMap* mb = &maps.b[p.seg[s].map_b];
+            const int lo = max(kb0 - seg_first, 0);
+            const int hi = min(kb1 - seg_first, kb_seg[s]);
+            for (int kb = lo; kb < hi; ++kb) {
+              if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
+                if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+                goto done;
+              }
+              ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+              ptx::tma_load_2d(sA + stage * C::A_BYTES, ma, &full[stage], kb * BK, m_blk * BM);
+              ptx::tma_load_2d(sB + stage * C::B_BYTES, mb, &full[stage], kb * BK, n_blk * BN);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+          int m_blk, n_blk, kb0, kb1;
+          if (!unit_range(u, m_blk, n_blk, kb0, kb1)) continue;
+          const int acc = local & 1;
+          const uint32_t acc_phase = (local >> 1) & 1;
+          ++local;
+          if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
+            if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            goto done;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          bool first = true;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!ptx::mbar_wait(&full[stage], phase)) {
+              if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+              goto done;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_u32(sA + stage * C::A_BYTES);
+            const uint32_t b_addr = ptx::smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + kk * 32),
+                            ptx::sdesc_kmajor_sw128(b_addr + kk * 32), idesc, first ? 0u : 1u);
+              first = false;
+            }
+            ptx::mma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          ptx::mma_commit(&tfull[acc]);
+        }
+      }
+    } else {
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      int local = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        int m_blk, n_blk, kb0, kb1;
+        if (!unit_range(u, m_blk, n_blk, kb0, kb1)) continue;
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        ++local;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
+          if (lane == 0 && p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          goto done;
+        }
+        ptx::tc_fence_after();
+        const int m = m_blk * BM + row;
+        const bool valid = m < M_act;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n0 = n_blk * BN + c * 32;
+          if (n0 >= p.N) break;  // uniform over the CTA
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(
+              tmem_base + static_cast<uint32_t>(acc * BN + c * 32) +
+                  (static_cast<uint32_t>(q * 32) << 16),
+              r);
+          ptx::tmem_wait_ld();
+          if (valid) epilogue_chunk<EPI>(p, m, n0, r, n0 + 32 <= p.N);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tempty[acc]);
+      }
+    }
+  }
+
+done:
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int STAGES, int EPI>
+twell_status launch(const GemmMaps& maps, const GemmArgs& a, const DeviceInfo& dev,
+                    cudaStream_t s) {
+  using Cc = Cfg<BN, STAGES>;
+  static_assert(Cc::SMEM <= 232448, "shared memory budget");
+  auto kern = gemm_kernel<BN, STAGES, EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cc::SMEM) !=
+      cudaSuccess)
+    return TWELL_ERR_CUDA;
+  const int num_m = (a.M + BM - 1) / BM;
+  const int num_n = (a.N + BN - 1) / BN;
+  const int units = num_m * num_n * (a.ksplit > 1 ? a.ksplit : 1);
+  if (units == 0) return TWELL_OK;
+  const int grid = units < dev.sm_count ? units : dev.sm_count;
+  kern<<<grid, kThreads, Cc::SMEM, s>>>(maps, a, num_m, num_n);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+template <int BN, int STAGES>
+twell_status launch_epi(const GemmMaps& maps, const GemmArgs& a, const DeviceInfo& dev,
+                        cudaStream_t s) {
+  switch (a.epi) {
+    case EPI_STORE: return launch<BN, STAGES, EPI_STORE>(maps, a, dev, s);
+    case EPI_ADD: return launch<BN, STAGES, EPI_ADD>(maps, a, dev, s);
+    case EPI_UP: return launch<BN, STAGES, EPI_UP>(maps, a, dev, s);
+    case EPI_DA: return launch<BN, STAGES, EPI_DA>(maps, a, dev, s);
+  }
+  return TWELL_ERR_INVALID;
+}
+
+// ------------------------------------------------------------- transposes
+
+template <int MODE>
+__global__ void __launch_bounds__(256) transpose_kernel(const TransposeArgs a) {
+  __shared__ float tile[32][33];
+  const int R_act = a.R_dyn ? min(a.R, *a.R_dyn) : a.R;
+  const int c0 = blockIdx.x * 32;
+  const int r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + ty + 8 * i;
+    const int c = c0 + tx;
+    float v = 0.0f;
+    if (r < R_act && c < a.C) {
+      const int64_t sr = a.row_idx ? a.row_idx[r] : r;
+      if (MODE == 0) {
+        v = bf16_val(static_cast<const uint16_t*>(a.src)[sr * a.lds + c]);
+      } else {
+        v = static_cast<const float*>(a.src)[sr * a.lds + c];
+        if (MODE == 2) v *= a.src2[static_cast<int64_t>(r) * a.lds2 + c];
+      }
+    }
+    tile[ty + 8 * i][tx] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c0 + ty + 8 * i;
+    const int r = r0 + tx;
+    if (c < a.C && r < a.R_pad) {
+      const float v = tile[tx][ty + 8 * i];
+      const int64_t o = static_cast<int64_t>(c) * a.ldo + r;
+      if (MODE == 0) {
+        a.out_hi[o] = bf16_bits(v);
+      } else {
+        uint16_t hi, lo;
+        split(v, hi, lo);
+        a.out_hi[o] = hi;
+        a.out_lo[o] = lo;
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+  const int R_act = a.R_dyn ? min(a.R, *a.R_dyn) : a.R;
+  const int per_row = MODE == 0 ? a.C / 8 : a.C / 4;
+  const long long total = static_cast<long long>(R_act) * per_row;
+  for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(v / per_row);
+    const int q = static_cast<int>(v % per_row);
+    const int64_t sr = a.row_idx ? a.row_idx[i] : i;
+    if (MODE == 0) {
+      const uint4 x = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) +
+                                                     sr * a.lds)[q];
+      reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(i) * a.ldo)[q] = x;
+    } else {
+      const float4 x =
+          reinterpret_cast<const float4*>(static_cast<const float*>(a.src) + sr * a.lds)[q];
+      uint16_t h[4], l[4];
+      split(x.x, h[0], l[0]);
+      split(x.y, h[1], l[1]);
+      split(x.z, h[2], l[2]);
+      split(x.w, h[3], l[3]);
+      uint16_t* o = a.out + static_cast<int64_t>(i) * a.ldo + 4 * q;
+      reinterpret_cast<uint2*>(o)[0] =
+          make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16),
+                     h[2] | (static_cast<uint32_t>(h[3]) << 16));
+      reinterpret_cast<uint2*>(o + a.C)[0] =
+          make_uint2(l[0] | (static_cast<uint32_t>(l[1]) << 16),
+                     l[2] | (static_cast<uint32_t>(l[3]) << 16));
+    }
+  }
+}
+
+}  // namespace
+
+twell_status gemm_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                      int64_t pitch, bool is_b_wide) {
+  return make_tmap_bf16_2d(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                           BK, is_b_wide ? 256 : BM, static_cast<uint64_t>(pitch));
+}
+
+int gemm_ksplit(int64_t tiles, int64_t k, const DeviceInfo& dev) {
+  const int64_t kb = (k + BK - 1) / BK;
+  int64_t split = (kb + 63) / 64;
+  while (split * 2 <= kb && tiles * split < 2 * dev.sm_count) split *= 2;
+  if (split > kb) split = kb;
+  return static_cast<int>(split < 1 ? 1 : split);
+}
+
+namespace {
+__global__ void __launch_bounds__(256) zero_rows_kernel(float* C, int64_t ldc,
+                                                        const int32_t* row_idx, int32_t R,
+                                                        const int32_t* R_dyn, int32_t N) {
+  const int R_act = R_dyn ? min(R, *R_dyn) : R;
+  const int i = blockIdx.x;
+  if (i >= R_act) return;
+  float* row = C + static_cast<int64_t>(row_idx ? row_idx[i] : i) * ldc;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = 0.0f;
+}
+}  // namespace
+
+twell_status zero_rows(float* C, int64_t ldc, const int32_t* row_idx, int32_t R,
+                       const int32_t* R_dyn, int32_t N, cudaStream_t s) {
+  if (R <= 0) return TWELL_OK;
+  zero_rows_kernel<<<R, 256, 0, s>>>(C, ldc, row_idx, R, R_dyn, N);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+twell_status gemm_run(const GemmMaps& maps, const GemmArgs& a, bool wide_n,
+                      const DeviceInfo& dev, cudaStream_t s) {
+  if (a.nseg < 1 || a.nseg > kGemmMaxSeg || a.M < 0 || a.N <= 0) return TWELL_ERR_INVALID;
+  if (a.ksplit > 1 && (a.epi == EPI_UP || a.epi == EPI_DA)) return TWELL_ERR_INVALID;
+  if (a.M == 0) return TWELL_OK;
+  return wide_n ? launch_epi<256, 4>(maps, a, dev, s) : launch_epi<128, 6>(maps, a, dev, s);
+}
+
+twell_status transpose_run(int mode, const TransposeArgs& a, cudaStream_t s) {
+  if (a.C <= 0 || a.R_pad <= 0) return TWELL_OK;
+  dim3 grid((a.C + 31) / 32, (a.R_pad + 31) / 32);
+  switch (mode) {
+    case 0: transpose_kernel<0><<<grid, 256, 0, s>>>(a); break;
+    case 1: transpose_kernel<1><<<grid, 256, 0, s>>>(a); break;
+    case 2: transpose_kernel<2><<<grid, 256, 0, s>>>(a); break;
+    default: return TWELL_ERR_INVALID;
+  }
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+twell_status gather_run(int mode, const GatherArgs& a, cudaStream_t s) {
+  if (a.R <= 0) return TWELL_OK;
+  const long long per_row = mode == 0 ? a.C / 8 : a.C / 4;
+  long long blocks = (static_cast<long long>(a.R) * per_row + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  if (mode == 0)
+    gather_kernel<0><<<static_cast<int>(blocks), 256, 0, s>>>(a);
+  else
+    gather_kernel<1><<<static_cast<int>(blocks), 256, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace twell

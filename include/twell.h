@@ -138,6 +138,109 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
                            const uint16_t* Wd, int32_t D, float* y, int32_t* status_dev,
                            void* stream);
 
+/*
+ * Hybrid training format (paper section 2.B.3): rows whose every tile count
+ * is at most the ELL capacity C stay in a compact ELL matrix; the other
+ * ("overflow") rows go to a dense backup.  Both lists are in ascending token
+ * order.  Reading: a row overflows iff some tile count exceeds C (a count of
+ * exactly C stays in ELL).
+ *   *n_ell, *n_dense          device int32 row counts (n_dense is the true
+ *                             number of overflow rows; rows past max_dense get
+ *                             no dense row and TWELL_FLAG_DENSE_FULL is set)
+ *   row_map[t]                i >= 0: ELL row i;  i < 0: dense row -(i+1)
+ *   ell_rows[i]               token of ELL row i, i < n_ell
+ *   ell_cnt[i*n_t + k]        count of ELL row i in tile k (<= C)
+ *   ell_col/ell_val[(i*n_t + k)*C + s]   its entries, ascending, s < count
+ *   dense_rows[i]             token of dense row i, i < min(n_dense, max_dense)
+ *   dense_h[i*F + j]          fp32 ReLU(z) of that token (zeros where inactive)
+ * Sizes: row_map, ell_rows [T] int32; ell_cnt [T][n_t] uint8;
+ * ell_col [T][n_t][C] uint8; ell_val [T][n_t][C] float (T rows reserved since
+ * every row may be an ELL row); dense_rows [max_dense] int32;
+ * dense_h [max_dense][F] float.
+ */
+typedef struct {
+  int32_t T;
+  int32_t F;
+  int32_t tile;       /* must be TWELL_TILE */
+  int32_t cap;        /* C: ELL slots per (row, tile), 1..tile */
+  int32_t max_dense;  /* rows reserved for the dense backup, >= 0 */
+  int32_t* n_ell;
+  int32_t* n_dense;
+  int32_t* row_map;
+  int32_t* ell_rows;
+  float* ell_val;
+  uint8_t* ell_col;
+  uint8_t* ell_cnt;
+  int32_t* dense_rows;
+  float* dense_h;
+} hybrid_t;
+
+/*
+ * TwELL -> hybrid conversion (paper section 2.B.3: a custom kernel converts
+ * TwELL to the hybrid format).  Reads the TwELL `h` (slots and spill) and
+ * fills `out` (out->T == h->T, out->F == h->F; C = out->cap may differ from
+ * h->width: entries beyond W come from the spill slices).  Row lists and
+ * counts are produced on the device; nothing is read back.
+ */
+twell_status twell_to_hybrid(const twell_t* h, const hybrid_t* out, int32_t* status_dev,
+                             void* stream);
+
+/* Workspace operations for twell_workspace_size. */
+enum { TWELL_WS_HYBRID_FWD = 1, TWELL_WS_HYBRID_BWD = 2 };
+
+/*
+ * Bytes of device workspace `op` needs for a hybrid of T rows, width d_model
+ * D, F columns, ELL capacity C and max_dense dense rows (0 on bad
+ * arguments).  The workspace is scratch the call overwrites; it must be
+ * 256-byte aligned and not shared by calls that may overlap on the GPU.
+ */
+size_t twell_workspace_size(int32_t op, int32_t T, int32_t D, int32_t F, int32_t cap,
+                            int32_t max_dense);
+
+/*
+ * Hybrid training forward (paper section 2.B.3: dense-to-sparse and
+ * sparse-to-dense matmuls over the hybrid format).
+ *   ELL rows (CUDA cores): u = x_t . W_u[:, j] at every ELL entry, saved in
+ *     u_ell (same layout as ell_val), and y_t = sum_j (h u) W_d[j, :].
+ *   Dense rows (tensor cores): U = X_ov W_u, saved in U_dense [max_dense][F]
+ *     fp32; y_ov = (H_ov * U) W_d with the fp32 product split into bf16 hi
+ *     and lo halves (two MMAs), so the bf16 operand adds no rounding beyond
+ *     about 2^-17 relative.
+ *   x [T][D] bf16; Wu_t, Wd [F][D] bf16; y [T][D] fp32 (every row written,
+ *   dense rows past max_dense excepted); u_ell [T][n_t][C] fp32;
+ *   ws: twell_workspace_size(TWELL_WS_HYBRID_FWD, ...) bytes (may be NULL
+ *   when max_dense == 0).  Dense rows of y sum split-K partial products with
+ *   atomics, so they agree across calls to fp32 rounding, not bit for bit.
+ */
+twell_status hybrid_ffn_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
+                            const uint16_t* Wd, int32_t D, float* y, float* u_ell,
+                            float* U_dense, void* ws, size_t ws_bytes, int32_t* status_dev,
+                            void* stream);
+
+/*
+ * Hybrid training backward with the L1 term (paper section 2.B.3; L1
+ * coefficient from the news article's recipe list).  For the loss
+ * L(y) + l1_coeff * sum(h), with dy = dL/dy [T][D] fp32 and a = h * u:
+ *   da = dy W_d^T;  du = da h;  dz = da u + l1_coeff at active entries;
+ *   dx = dz W_g^T + du W_u^T;  dW_g^T = dz^T x;  dW_u^T = du^T x;
+ *   dW_d = a^T dy.
+ * ELL rows run on the CUDA cores (dense-to-sparse da, sparse-to-dense dx,
+ * per-neuron records for the weight gradients); dense rows run on the tensor
+ * cores with fp32 operands split into bf16 hi and lo halves.
+ *   u_ell, U_dense   as written by hybrid_ffn_fwd for the same hybrid
+ *   dx [T][D] fp32 (written);  dWg_t, dWu_t, dWd [F][D] fp32 (overwritten,
+ *   not accumulated, in the weights' neuron-major layout)
+ *   ws: twell_workspace_size(TWELL_WS_HYBRID_BWD, ...) bytes
+ * The weight gradients sum per-neuron records in an order set by atomics,
+ * and dense rows sum split-K partial products with atomics, so repeated
+ * calls agree to fp32 rounding, not bit for bit.
+ */
+twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, const float* u_ell,
+                            const float* U_dense, const uint16_t* Wg_t, const uint16_t* Wu_t,
+                            const uint16_t* Wd, int32_t D, const float* dy, float l1_coeff,
+                            float* dx, float* dWg_t, float* dWu_t, float* dWd, void* ws,
+                            size_t ws_bytes, int32_t* status_dev, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* twell_status_string(twell_status s);
 

@@ -1,0 +1,250 @@
+"""GPU parity of the training path through the C-ABI: TwELL -> hybrid
+conversion (bit-exact against the oracle fed the kernel's own gate
+pre-activations), the hybrid forward and the hybrid backward with the L1
+term (against the dense fp64 oracle, max-abs <= 2e-2 * RMS per tensor)."""
+import numpy as np
+import pytest
+import torch
+
+import activation_sparse_gated_gate_gb300 as tw
+import oracle
+import workloads
+from _gpu import ensure_built, run_pack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _hybrid_case(w, cap, max_dense=None, spill_cap=None):
+    d, h, z = run_pack(w, spill_cap=spill_cap)
+    hyb = tw.Hybrid(w.T, w.F, cap, w.T if max_dense is None else max_dense)
+    tw.twell_to_hybrid(h, hyb)
+    torch.cuda.synchronize()
+    zg = z.cpu().numpy()
+    ref = oracle.to_hybrid(oracle.twell_pack(zg, 128, w.width), cap)
+    return d, h, hyb, zg, ref
+
+
+def _assert_hybrid_equal(hyb, ref, max_dense):
+    n_ell, n_dense = hyb.n_ell, hyb.n_dense
+    assert n_ell == len(ref.ell_rows) and n_dense == len(ref.dense_rows)
+    np.testing.assert_array_equal(hyb.ell_rows[:n_ell].cpu().numpy(), ref.ell_rows)
+    np.testing.assert_array_equal(hyb.row_map[:hyb.T].cpu().numpy(), ref.row_map)
+    cnt = hyb.ell_cnt[:n_ell].cpu().numpy().astype(np.int64)
+    np.testing.assert_array_equal(cnt, ref.ell_cnt)
+    s = np.arange(hyb.cap)[None, None, :]
+    used = s < cnt[:, :, None]
+    gcol = hyb.ell_col[:n_ell].cpu().numpy().astype(np.int64)
+    np.testing.assert_array_equal(np.where(used, gcol, -1),
+                                  np.where(used, ref.ell_col, -1))
+    np.testing.assert_array_equal(np.where(used, hyb.ell_val[:n_ell].cpu().numpy(), 0),
+                                  np.where(used, ref.ell_val, 0))
+    nd = min(n_dense, max_dense)
+    np.testing.assert_array_equal(hyb.dense_rows[:nd].cpu().numpy(), ref.dense_rows[:nd])
+    np.testing.assert_array_equal(hyb.dense_h[:nd].cpu().numpy(), ref.dense_h[:nd])
+
+
+@pytest.mark.parametrize("T,D,F,p,W,cap", [
+    (300, 128, 1024, 0.05, 8, 8),      # C == W
+    (257, 64, 512, 0.10, 8, 16),       # C > W: ELL entries from spill slices
+    (200, 128, 640, 0.10, 16, 8),      # C < W
+    (64, 64, 256, 0.001, 8, 8),        # almost nothing active
+    (96, 64, 256, 0.6, 8, 8),          # almost every row overflows
+])
+def test_to_hybrid_bit_exact(T, D, F, p, W, cap):
+    w = workloads.random_small(T, D, F, p, W, seed=T + F)
+    _, h, hyb, zg, ref = _hybrid_case(w, cap)
+    _assert_hybrid_equal(hyb, ref, T)
+    assert int(hyb.status.item()) == 0
+
+
+def test_to_hybrid_training_config_rows():
+    # the training workload's construction at reduced T: the forced rows
+    # (40% dense) and only they overflow C = 32
+    w = workloads.config(3, T=2048)
+    _, h, hyb, zg, ref = _hybrid_case(w, 32, max_dense=256)
+    _assert_hybrid_equal(hyb, ref, 256)
+    assert hyb.n_dense == round(0.03 * 2048)
+
+
+def test_to_hybrid_dense_capacity_exhausted_sets_flag():
+    w = workloads.random_small(128, 64, 512, 0.4, 8, seed=9)
+    _, h, hyb, zg, ref = _hybrid_case(w, 8, max_dense=4)
+    assert len(ref.dense_rows) > 4
+    assert int(hyb.status.item()) & tw.FLAG_DENSE_FULL
+    _assert_hybrid_equal(hyb, ref, 4)
+
+
+# --------------------------------------------------------------- hybrid forward
+
+from _gpu import check_y  # noqa: E402
+
+TRAIN_SMALL = [
+    # T, D, F, mean density, dense fraction, dense density, C, max_dense
+    (512, 128, 1024, 0.05, 0.05, 0.4, 8, 512),
+    (1000, 256, 2048, 0.05, 0.03, 0.4, 16, 256),    # ragged T, >1 row tile
+    (300, 72, 384, 0.08, 0.10, 0.5, 8, 300),        # D not a multiple of 64
+]
+
+
+def _training(T, D, F, p, frac, pd, cap, seed=0):
+    return workloads.make_training(f"train {T}x{D}x{F}", T, D, F, p, frac, pd, cap,
+                                   2e-5, seed=seed)
+
+
+def _fwd(w, max_dense):
+    d, h, hyb, zg, ref = _hybrid_case(w, w.cap, max_dense=max_dense)
+    y, u_ell, U_dense = tw.hybrid_ffn_fwd(d["x"], hyb, d["Wu_t"], d["Wd"])
+    torch.cuda.synchronize()
+    return d, h, hyb, zg, ref, y, u_ell, U_dense
+
+
+def _check_u(w, hyb, ref, u_ell, U_dense):
+    X = oracle.bf16_to_f64(w.x)
+    U = oracle.bf16_to_f64(w.Wu_t)
+    n_ell = hyb.n_ell
+    ue = u_ell[:n_ell].cpu().numpy().astype(np.float64)
+    cnt = ref.ell_cnt
+    eps = 2.0 ** -24
+    for i, t in enumerate(ref.ell_rows):
+        ks, ss = np.nonzero(np.arange(hyb.cap)[None, :] < cnt[i][:, None])
+        js = ks * 128 + ref.ell_col[i, ks, ss]
+        uref = U[js] @ X[t]
+        bound = w.D * eps * (np.abs(U[js]) @ np.abs(X[t])) + 1e-30
+        assert (np.abs(ue[i, ks, ss] - uref) <= bound).all(), f"u at ELL row {i}"
+    nd = min(hyb.n_dense, hyb.max_dense)
+    if nd:
+        rows = ref.dense_rows[:nd]
+        Ug = U_dense[:nd].cpu().numpy().astype(np.float64)
+        uref = X[rows] @ U.T
+        bound = w.D * eps * (np.abs(X[rows]) @ np.abs(U).T) + 1e-30
+        assert (np.abs(Ug - uref) <= bound).all(), "U of dense rows"
+
+
+@pytest.mark.parametrize("T,D,F,p,frac,pd,cap,md", TRAIN_SMALL)
+def test_hybrid_fwd_parity(T, D, F, p, frac, pd, cap, md):
+    w = _training(T, D, F, p, frac, pd, cap, seed=T)
+    d, h, hyb, zg, ref, y, u_ell, U_dense = _fwd(w, md)
+    assert int(hyb.status.item()) == 0
+    assert hyb.n_dense > 0
+    check_y(y.cpu().numpy().astype(np.float64), w, zg)
+    _check_u(w, hyb, ref, u_ell, U_dense)
+
+
+def test_hybrid_fwd_training_config_reduced():
+    w = workloads.config(3, T=2048)
+    d, h, hyb, zg, ref, y, u_ell, U_dense = _fwd(w, 128)
+    assert int(hyb.status.item()) == 0
+    check_y(y.cpu().numpy().astype(np.float64), w, zg)
+    _check_u(w, hyb, ref, u_ell, U_dense)
+
+
+# -------------------------------------------------------------- hybrid backward
+
+def _bwd(w, max_dense, l1, dy=None):
+    d, h, hyb, zg, ref, y, u_ell, U_dense = _fwd(w, max_dense)
+    dyt = torch.from_numpy(w.dy if dy is None else dy).cuda()
+    grads = tw.hybrid_ffn_bwd(d["x"], hyb, u_ell, U_dense, d["Wg_t"], d["Wu_t"], d["Wd"], dyt,
+                              l1)
+    torch.cuda.synchronize()
+    assert int(hyb.status.item()) == 0
+    return zg, [g.cpu().numpy().astype(np.float64) for g in grads]
+
+
+def _grad_check(got, ref, names, tight=2e-3, scales=None):
+    """Spec bar (max-abs <= 2e-2 * RMS) plus a much tighter
+    bug-catching bar, |err| <= 2e-3 RMS + 2e-5 |ref|: fp32 arithmetic with
+    bf16 hi/lo tensor-core operands lands far inside it; the relative term
+    covers the fp32 tensor-core accumulation on outlier elements (the bias
+    feature's column of dx reaches ~260 RMS)."""
+    from _gpu import rms
+    for i, (g, r, n) in enumerate(zip(got, ref, names)):
+        scale = rms(r) if scales is None else scales[i]
+        err = float(np.max(np.abs(g - r)))
+        assert err <= 2e-2 * scale, f"{n}: max-abs {err:.3e} > 2e-2*RMS {2e-2 * scale:.3e}"
+        excess = np.abs(g - r) - (tight * scale + 2e-5 * np.abs(r))
+        assert (excess <= 0).all(), f"{n}: tight bar exceeded by {float(excess.max()):.3e}"
+
+
+NAMES = ("dx", "dWg_t", "dWu_t", "dWd")
+
+
+@pytest.mark.parametrize("T,D,F,p,frac,pd,cap,md", TRAIN_SMALL)
+def test_hybrid_bwd_parity(T, D, F, p, frac, pd, cap, md):
+    w = _training(T, D, F, p, frac, pd, cap, seed=T)
+    zg, got = _bwd(w, md, 2e-5)
+    ref = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, w.dy, 2e-5, active=zg > 0)
+    _grad_check(got, ref, NAMES)
+
+
+@pytest.mark.parametrize("lam", [2e-5, 1.0])
+def test_hybrid_bwd_l1_term_alone(lam):
+    # dy = 0 leaves only the L1 term: dx_t = lambda sum_{active j} W_g[:, j],
+    # dW_g[:, j] = lambda sum_{active t} x_t, dW_u = dW_d = 0
+    w = _training(400, 128, 1024, 0.05, 0.05, 0.4, 8, seed=11)
+    zg, got = _bwd(w, 400, lam, dy=np.zeros_like(w.dy))
+    ref = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, np.zeros_like(w.dy), lam,
+                              active=zg > 0)
+    for g, r, n in zip(got[:2], ref[:2], NAMES[:2]):
+        err = np.max(np.abs(g - r))
+        assert err <= 1e-5 * np.max(np.abs(r)), f"{n}: {err:.3e}"
+    assert np.abs(got[0]).max() > 0
+    assert not got[2].any() and not got[3].any()
+
+
+def test_hybrid_bwd_lambda_zero_is_plain_gradient():
+    w = _training(300, 128, 1024, 0.05, 0.05, 0.4, 8, seed=12)
+    zg, got = _bwd(w, 300, 0.0)
+    ref = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, w.dy, 0.0, active=zg > 0)
+    _grad_check(got, ref, NAMES)
+
+
+def test_hybrid_bwd_training_config_reduced():
+    w = workloads.config(3, T=2048)
+    zg, got = _bwd(w, 128, w.l1_coeff)
+    ref = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, w.dy, w.l1_coeff, active=zg > 0)
+    _grad_check(got, ref, NAMES)
+
+
+def test_training_config_full_size():
+    """The 2B-class training step at full size (T=16384, D=2304, F=9216,
+    C=32) in the bench's launch configuration; y and dx checked on sampled
+    token rows, the weight gradients on sampled neurons (each depends on its
+    own row / neuron alone).  The RMS scale of each tensor is the kernel's
+    full tensor (a sample cannot give the reference's)."""
+    from _gpu import rms
+    w = workloads.config(3)
+    d, h, z = run_pack(w)
+    hyb = tw.Hybrid(w.T, w.F, w.cap, 1024)
+    tw.twell_to_hybrid(h, hyb)
+    y, u_ell, U_dense = tw.hybrid_ffn_fwd(d["x"], hyb, d["Wu_t"], d["Wd"])
+    dyt = torch.from_numpy(w.dy).cuda()
+    grads = tw.hybrid_ffn_bwd(d["x"], hyb, u_ell, U_dense, d["Wg_t"], d["Wu_t"], d["Wd"], dyt,
+                              w.l1_coeff)
+    torch.cuda.synchronize()
+    assert int(hyb.status.item()) == 0 and int(h.status.item()) == 0
+    assert hyb.n_dense == round(0.03 * w.T)
+    rng = np.random.default_rng(3)
+    dense = hyb.dense_rows[:hyb.n_dense].cpu().numpy()
+    rows = np.sort(np.concatenate([rng.choice(w.T, 40, replace=False), dense[:8]]))
+    zr = z[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+    yg = y[torch.as_tensor(rows, device="cuda")].cpu().numpy().astype(np.float64)
+    yref = oracle.ffn_forward(w.x[rows], w.Wg_t, w.Wu_t, w.Wd, active=zr > 0)
+    dxg = grads[0][torch.as_tensor(rows, device="cuda")].cpu().numpy().astype(np.float64)
+    dxref = oracle.ffn_backward_dx_rows(w.x, w.Wg_t, w.Wu_t, w.Wd, w.dy, w.l1_coeff, rows,
+                                        active_rows=zr > 0)
+    full = [y, grads[0]]
+    _grad_check([yg, dxg], [yref, dxref], ("y", "dx"),
+                scales=[float(torch.sqrt((t.double() ** 2).mean())) for t in full])
+    neurons = np.sort(rng.choice(w.F, 24, replace=False))
+    zc = z[:, torch.as_tensor(neurons, device="cuda")].cpu().numpy()
+    refw = oracle.ffn_backward_dw_cols(w.x, w.Wg_t, w.Wu_t, w.Wd, w.dy, w.l1_coeff, neurons,
+                                       active_cols=zc > 0)
+    gotw = [g[torch.as_tensor(neurons, device="cuda")].cpu().numpy().astype(np.float64)
+            for g in grads[1:]]
+    _grad_check(gotw, refw, NAMES[1:],
+                scales=[float(torch.sqrt((g.double() ** 2).mean())) for g in grads[1:]])

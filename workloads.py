@@ -184,6 +184,8 @@ def make_training(name, T, D, F, mean_density, dense_frac, dense_density, cap,
     n_dense = int(round(dense_frac * T))
     dense_rows = rng.choice(T, n_dense, replace=False) if n_dense else np.zeros(0, np.int64)
     p_base = (mean_density * T - dense_density * n_dense) / (T - n_dense)
+    if not 0.0 < p_base < 1.0:
+        raise ValueError(f"no base density gives mean {mean_density} (base {p_base})")
     tau_b = threshold_for_density(p_base, D)
     tau_d = threshold_for_density(dense_density, D)
     x[:, D - 1] = tau_b
