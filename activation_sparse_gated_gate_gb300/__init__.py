@@ -18,7 +18,8 @@ import torch
 
 __all__ = [
     "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
-    "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_bwd",
+    "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
+    "hybrid_ffn_bwd",
     "twell_status_string",
     "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "TILE",
 ]
@@ -75,6 +76,8 @@ _SIGNATURES = {
     "hybrid_ffn_bwd": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_ptr, c_ptr,
                                c_ptr, c_i32, c_ptr, ctypes.c_float, c_ptr, c_ptr, c_ptr, c_ptr,
                                c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "hybrid_ffn_fwd_noalloc": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_i32,
+                                       c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "twell_status_string": (ctypes.c_char_p, [c_i32]),
     "twell_version": (c_i32, []),
 }
@@ -308,3 +311,28 @@ def hybrid_ffn_bwd(x, h: Hybrid, u_ell, U_dense, Wg_t, Wu_t, Wd, dy, l1_coeff, d
                                     _stream(stream)),
                "hybrid_ffn_bwd")
     return dx, dWg_t, dWu_t, dWd
+
+
+def hybrid_ffn_fwd_noalloc(x, h: Hybrid, Wu_t, Wd, y=None, u_ell=None, U_dense=None,
+                           status=None, stream=None):
+    """hybrid_ffn_fwd with the library's own 64 MiB device scratch array as
+    workspace (for callers that cannot allocate device memory); returns
+    (y, u_ell, U_dense).  Outputs are still the caller's."""
+    _need(x, torch.bfloat16, "x")
+    _need(Wu_t, torch.bfloat16, "Wu_t")
+    _need(Wd, torch.bfloat16, "Wd")
+    T, D = x.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    if u_ell is None:
+        u_ell = torch.empty((T, h.n_t, h.cap), dtype=torch.float32, device=dev)
+    if U_dense is None:
+        U_dense = torch.empty((max(h.max_dense, 1), h.F), dtype=torch.float32, device=dev)
+    status = h.status if status is None else status
+    with torch.cuda.device(dev):
+        _check(lib().hybrid_ffn_fwd_noalloc(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t),
+                                            _ptr(Wd), D, _ptr(y), _ptr(u_ell), _ptr(U_dense),
+                                            _ptr(status), _stream(stream)),
+               "hybrid_ffn_fwd_noalloc")
+    return y, u_ell, U_dense

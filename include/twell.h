@@ -241,6 +241,26 @@ twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, const float* u
                             float* dx, float* dWg_t, float* dWu_t, float* dWd, void* ws,
                             size_t ws_bytes, int32_t* status_dev, void* stream);
 
+/*
+ * hybrid_ffn_fwd with no workspace argument, for callers that cannot
+ * allocate device memory themselves (a loop whose memory budget is fixed up
+ * front, a host program without access to a device allocator, code that must
+ * not call cudaMalloc because it can synchronise the device).  The paper has
+ * no counterpart: this is a packaging of hybrid_ffn_fwd, with the same
+ * arguments, results and errors apart from the workspace.
+ *   The workspace is a 64 MiB device array inside this library, held on
+ *   every GPU that loads it until the process exits.  A hybrid whose
+ *   forward workspace (twell_workspace_size(TWELL_WS_HYBRID_FWD, ...)) is
+ *   larger returns TWELL_ERR_UNSUPPORTED and enqueues nothing.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  The entry point allocates nothing.
+ *   All calls share the array: calls that may overlap on the GPU race.
+ */
+twell_status hybrid_ffn_fwd_noalloc(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
+                                    const uint16_t* Wd, int32_t D, float* y, float* u_ell,
+                                    float* U_dense, int32_t* status_dev, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* twell_status_string(twell_status s);
 
