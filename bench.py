@@ -104,6 +104,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value, device=None):
+    """Max of a per-rank float over the process group (the identity without
+    one).  The timed region's length is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world_size, max_ms_per_step):
+    """Whole-job throughput of replicas: every rank processes its own batch
+    of `tokens_per_rank` tokens per step; the step takes the slowest rank's
+    time."""
+    return world_size * tokens_per_rank / (max_ms_per_step / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -173,6 +192,85 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------ GPU path
 
+def run_train(args, dev, flush, stream):
+    """Training step of the 2B-class layer (T=16384, D=2304, F=9216, mean 5%
+    active, 3% of rows above the ELL capacity C=32): gate GEMM with TwELL
+    epilogue (W=32), TwELL->hybrid, hybrid forward, hybrid backward with the
+    L1 term.  Returns a dict for the JSON line (per-kernel event times)."""
+    import torch
+
+    import activation_sparse_gated_gate_gb300 as tw
+    import workloads
+
+    w = workloads.config(3)
+
+    def up(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    x, Wg, Wu, Wd = up(w.x), up(w.Wg_t), up(w.Wu_t), up(w.Wd)
+    dy = torch.from_numpy(w.dy).to(dev)
+    max_dense = 1024
+    h = tw.TwELL(w.T, w.F, w.cap, device=dev)
+    hyb = tw.Hybrid(w.T, w.F, w.cap, max_dense, device=dev)
+    f32 = torch.float32
+    y = torch.empty((w.T, w.D), dtype=f32, device=dev)
+    u_ell = torch.empty((w.T, w.F // 128, w.cap), dtype=f32, device=dev)
+    U_dense = torch.empty((max_dense, w.F), dtype=f32, device=dev)
+    dx = torch.empty((w.T, w.D), dtype=f32, device=dev)
+    dW = [torch.empty((w.F, w.D), dtype=f32, device=dev) for _ in range(3)]
+    ws_f = tw._workspace(tw.twell_workspace_size(tw.WS_HYBRID_FWD, w.T, w.D, w.F, w.cap,
+                                                 max_dense), dev)
+    ws_b = tw._workspace(tw.twell_workspace_size(tw.WS_HYBRID_BWD, w.T, w.D, w.F, w.cap,
+                                                 max_dense), dev)
+    names = ["twell_gate_pack", "twell_to_hybrid", "hybrid_ffn_fwd", "hybrid_ffn_bwd"]
+
+    def launch(i):
+        if i == 0:
+            tw.twell_gate_pack(x, Wg, h, stream=stream)
+        elif i == 1:
+            tw.twell_to_hybrid(h, hyb, stream=stream)
+        elif i == 2:
+            tw.hybrid_ffn_fwd(x, hyb, Wu, Wd, y=y, u_ell=u_ell, U_dense=U_dense, ws=ws_f,
+                              stream=stream)
+        else:
+            tw.hybrid_ffn_bwd(x, hyb, u_ell, U_dense, Wg, Wu, Wd, dy, w.l1_coeff, dx=dx,
+                              dWg_t=dW[0], dWu_t=dW[1], dWd=dW[2], ws=ws_b, stream=stream)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        for i in range(4):
+            launch(i)
+    torch.cuda.synchronize()
+    if int(h.status.item()) or int(hyb.status.item()):
+        raise RuntimeError("device status flags set in the training step")
+    K = args.train_steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        for i in range(4):
+            launch(i)
+            ev[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = {n: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+           for i, n in enumerate(names)}
+    ms = max_over_ranks(sum(per.values()), dev)
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    nnz = int(h.cnt.to(torch.int64).sum().item())
+    return {
+        "metric": "sparse gated-FFN training step (fwd+bwd) tokens/s per layer",
+        "value": job_tokens_per_s(w.T, ws, ms), "unit": "tokens/s", "ms_per_step": ms,
+        "steps": K, "scaling": "weak",
+        "dtype": "bf16 in, fp32 accumulate / gradients",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F, "cap": w.cap,
+                   "l1_coeff": w.l1_coeff, "nnz": nnz, "density": nnz / (w.T * w.F),
+                   "n_dense": hyb.n_dense, "max_dense": max_dense,
+                   "l2": "flushed (512 MiB write) before every step"},
+        "kernels_ms": per,
+    }
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -231,13 +329,9 @@ def run_ours(args, w):
         dist.barrier()
     t_k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     t_k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    total_ms = sum(a + b for a, b in zip(t_k1, t_k2))
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(a + b for a, b in zip(t_k1, t_k2)), dev)
     ms_step = total_ms / K
-    value = ws * w.T / (total_ms / K / 1e3)
+    value = job_tokens_per_s(w.T, ws, ms_step)
 
     # end to end through the public API with host buffers: pinned x in, y out
     xh = x.cpu().pin_memory()
@@ -251,11 +345,7 @@ def run_ours(args, w):
         yh.copy_(y, non_blocking=True)
         e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e_ev) / K
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e_ev) / K, dev)
     h2d = x.numel() * 2
     d2h = y.numel() * 4
 
@@ -294,13 +384,16 @@ def run_ours(args, w):
                    "l2": ("NOT flushed (profiling run)" if args.no_flush
                           else "flushed (512 MiB write) before every step"),
                    "parallelism": f"replicas x{ws}"},
-        "e2e": {"value": ws * w.T / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(w.T, ws, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 2 * K,
         "roofline": roof,
         "kernels": kernels,
         "clocks": clk.summary(),
     }
+    if not args.no_train:
+        out["train"] = run_train(args, dev, flush, stream)
+        out["train"]["n_gpus"] = ws
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, n, s = time_oracle(w, budget_s=args.ref_budget)
         out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
@@ -323,6 +416,8 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="token count override")
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-train", action="store_true", help="skip the training-step section")
+    ap.add_argument("--train-steps", type=int, default=5)
     ap.add_argument("--no-flush", action="store_true",
                     help="skip the L2 flush (profiling runs only; not a valid bench number)")
     args = ap.parse_args()
