@@ -8,8 +8,8 @@
 // many tokens G covers the whole row and the warp stores y_t; with few
 // tokens (decode) rows are split into several units so every SM gets work,
 // and each unit adds its partial y_t with 16-byte atomics into a zeroed y.
-// x_t (fp32) and the fp32 accumulator of y_t live in registers, spread over
-// the 32 lanes in 8-element chunks (lane l holds chunks l, l+32, ...).
+// x_t (bf16 pairs) and the fp32 accumulator of y_t live in registers, spread
+// over the 32 lanes in 8-element chunks (lane l holds chunks l, l+32, ...).
 //
 // Per unit the warp first lists its active entries (j, h) in shared memory:
 // the counts of 32 tiles are read at once, a warp prefix sum places every
@@ -18,9 +18,11 @@
 // stages: lane 0 issues two cp.async.bulk copies per entry (neuron j's rows
 // W_u^T[j] and W_d[j], 2*D contiguous bf16 each) completing on the stage's
 // mbarrier, P entries ahead of the compute.  Per entry the lanes read the
-// staged rows with 16-byte shared loads, form u = x_t . W_u[:, j] with four
-// independent partial sums and a butterfly reduction, and accumulate
-// (h u) W_d[j, :].
+// staged rows with 16-byte shared loads, form u = x_t . W_u[:, j] with the
+// mixed-precision FMA (bf16 x bf16 products into eight independent fp32
+// sums: x_t and W_u stay bf16, nothing is widened) and a butterfly
+// reduction, and accumulate (h u) W_d[j, :] with the packed fp32-pair FMA
+// (fma.rn.f32x2) on W_d's bf16 pairs widened to fp32 pairs.
 #include "fused.cuh"
 #include "ptx.cuh"
 
@@ -34,6 +36,38 @@ constexpr int kSmemBudget = 220 * 1024;
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// fp32 pairs in a 64-bit register pair, for the packed pair FMA (sm_100+)
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + d on fp32 pairs
+__device__ __forceinline__ void fma2(f32x2& d, f32x2 a, f32x2 b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+// lo += a.lo * b.lo, hi += a.hi * b.hi on bf16 pairs: bf16 x bf16 products,
+// fp32 addends and results (mixed-precision FMA)
+__device__ __forceinline__ void dot_bf16x2(float& lo, float& hi, uint32_t a, uint32_t b) {
+  asm("{\n"
+      ".reg .b16 al, ah, bl, bh;\n"
+      "mov.b32 {al, ah}, %2;\n"
+      "mov.b32 {bl, bh}, %3;\n"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n"
+      "fma.rn.f32.bf16 %1, ah, bh, %1;\n"
+      "}\n"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
 
 // NC = 8-element chunks per lane (D <= 256 * NC).  EXACT: D == 256 * NC, so
 // every lane owns all NC of its chunks.
@@ -79,7 +113,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
     const int t = ELL ? p.ell_rows[row] : row;
     const int k_begin = static_cast<int>(u % p.upr) * p.G;
     const int k_end = min(k_begin + p.G, p.n_t);
-    float xf[NC][8];
+    uint32_t xb[NC][4];
     float acc[NC][8];
     bool have_x = false;
     bool any = false;
@@ -120,12 +154,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
         for (int i = 0; i < NC; ++i) {
           uint4 v = own(i) ? __ldg(reinterpret_cast<const uint4*>(xr + 8 * (lane + 32 * i)))
                            : make_uint4(0, 0, 0, 0);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            xf[i][2 * e] = bf16lo(w4[e]);
-            xf[i][2 * e + 1] = bf16hi(w4[e]);
-          }
+          xb[i][0] = v.x;
+          xb[i][1] = v.y;
+          xb[i][2] = v.z;
+          xb[i][3] = v.w;
         }
       }
 
@@ -170,24 +202,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
           const uint4* su =
               reinterpret_cast<const uint4*>(stages + static_cast<size_t>(s) * 2 * row_bytes);
           const uint4* sd = su + nch;
-          float pp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          float pp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int q = 0; q < NC; ++q) {
             if (own(q)) {
               const uint4 a = su[lane + 32 * q];
               const uint32_t a4[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-              for (int r = 0; r < 4; ++r) {
-                pp[r] = fmaf(xf[q][2 * r], bf16lo(a4[r]), pp[r]);
-                pp[r] = fmaf(xf[q][2 * r + 1], bf16hi(a4[r]), pp[r]);
-              }
+              for (int r = 0; r < 4; ++r) dot_bf16x2(pp[2 * r], pp[2 * r + 1], xb[q][r], a4[r]);
             }
           }
-          float part = (pp[0] + pp[1]) + (pp[2] + pp[3]);
+          float part = ((pp[0] + pp[1]) + (pp[2] + pp[3])) + ((pp[4] + pp[5]) + (pp[6] + pp[7]));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
           if (ELL && lane == 0) p.u_save[e.pos] = part;
           const float sc = e.h * part;
+          const f32x2 sc2 = pack2(sc, sc);
 #pragma unroll
           for (int q = 0; q < NC; ++q) {
             if (own(q)) {
@@ -195,8 +225,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
               const uint32_t b4[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
               for (int r = 0; r < 4; ++r) {
-                acc[q][2 * r] = fmaf(sc, bf16lo(b4[r]), acc[q][2 * r]);
-                acc[q][2 * r + 1] = fmaf(sc, bf16hi(b4[r]), acc[q][2 * r + 1]);
+                f32x2 a2 = pack2(acc[q][2 * r], acc[q][2 * r + 1]);
+                fma2(a2, sc2, pack2(bf16lo(b4[r]), bf16hi(b4[r])));
+                unpack2(a2, acc[q][2 * r], acc[q][2 * r + 1]);
               }
             }
           }
