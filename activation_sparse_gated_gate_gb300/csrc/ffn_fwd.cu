@@ -4,7 +4,8 @@
 // products only for the nonzero elements and keeping DRAM traffic low).
 //
 // Work unit = (token row t, range of G column tiles); one warp per unit at a
-// time (8 warps per CTA, one CTA per SM, units strided over the grid).  With
+// time (12 warps per CTA for D <= 1536, else 8; one CTA per SM; units
+// strided over the grid).  With
 // many tokens G covers the whole row and the warp stores y_t; with few
 // tokens (decode) rows are split into several units so every SM gets work,
 // and each unit adds its partial y_t with 16-byte atomics into a zeroed y.
@@ -29,8 +30,12 @@
 namespace twell {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kListCap = 256;        // entries listed per pass
+constexpr int kListCap = 128;        // entries listed per pass
+
+// Warps per CTA (one CTA per SM): 12 while a thread's row state fits in
+// 65536 / 384 registers (D <= 1536; measured 271 us against 324 us with 8
+// warps at the 0.5B-class shape), else 8.
+__host__ __device__ constexpr int warps_for(int nc) { return nc <= 6 ? 12 : 8; }
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 220 * 1024;
 
@@ -72,7 +77,8 @@ __device__ __forceinline__ void dot_bf16x2(float& lo, float& hi, uint32_t a, uin
 // NC = 8-element chunks per lane (D <= 256 * NC).  EXACT: D == 256 * NC, so
 // every lane owns all NC of its chunks.
 template <int NC, bool EXACT, bool ELL>
-__global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams p) {
+__global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const FfnParams p) {
+  constexpr int kWarps = warps_for(NC);
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -270,6 +276,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ffn_fwd_kernel(const FfnParams
 
 template <int NC, bool ELL>
 twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
+  constexpr int kWarps = warps_for(NC);
   const int stage_bytes = 4 * p.D;
   const int fixed = kMaxStages * 8 + kListCap * static_cast<int>(sizeof(Entry));
   int P = (kSmemBudget / kWarps - fixed) / stage_bytes;
