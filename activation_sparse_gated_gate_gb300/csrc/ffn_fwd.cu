@@ -4,7 +4,7 @@
 // products only for the nonzero elements and keeping DRAM traffic low).
 //
 // Work unit = (token row t, range of G column tiles); one warp per unit at a
-// time (12 warps per CTA for D <= 1536, else 8; one CTA per SM; units
+// time (12 warps per CTA for D <= 2304, else 8; one CTA per SM; units
 // strided over the grid).  With
 // many tokens G covers the whole row and the warp stores y_t; with few
 // tokens (decode) rows are split into several units so every SM gets work,
@@ -30,14 +30,15 @@
 namespace twell {
 namespace {
 
-constexpr int kListCap = 128;        // entries listed per pass
+constexpr int kListCap = 64;         // entries listed per pass
 
 // Warps per CTA (one CTA per SM): 12 while a thread's row state fits in
-// 65536 / 384 registers (D <= 1536; measured 271 us against 324 us with 8
-// warps at the 0.5B-class shape), else 8.
-__host__ __device__ constexpr int warps_for(int nc) { return nc <= 6 ? 12 : 8; }
+// 65536 / 384 registers without spills (D <= 2304), else 8.  Measured with
+// CUDA events: 0.5B-class shape 324 -> 271 us, 1.5B-class 1377 -> 1123 us,
+// 2B-class ELL forward 4.13 -> 3.35 ms against 8 warps.
+__host__ __device__ constexpr int warps_for(int nc) { return nc <= 9 ? 12 : 8; }
 constexpr int kMaxStages = 8;
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kSmemBudget = 231168;  // within the 227 KB opt-in limit
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -279,7 +280,8 @@ twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
   constexpr int kWarps = warps_for(NC);
   const int stage_bytes = 4 * p.D;
   const int fixed = kMaxStages * 8 + kListCap * static_cast<int>(sizeof(Entry));
-  int P = (kSmemBudget / kWarps - fixed) / stage_bytes;
+  const int budget = kSmemBudget < dev.max_smem_optin ? kSmemBudget : dev.max_smem_optin;
+  int P = (budget / kWarps - fixed) / stage_bytes;
   if (P > kMaxStages) P = kMaxStages;
   if (P < 1) return TWELL_ERR_UNSUPPORTED;
   p.stages = P;

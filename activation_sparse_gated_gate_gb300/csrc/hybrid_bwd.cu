@@ -36,10 +36,10 @@
 namespace twell {
 namespace {
 
-constexpr int kWarps = 6;
-constexpr int kListCap = 256;
+constexpr int kWarps = 8;
+constexpr int kListCap = 64;
 constexpr int kMaxStages = 8;
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kSmemBudget = 231168;  // within the 227 KB opt-in limit
 
 struct BwdParams {
   const uint16_t* x;
@@ -76,6 +76,26 @@ struct BEntry {
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// fp32 pairs in a 64-bit register pair, for the packed pair FMA (sm_100+)
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + d on fp32 pairs
+__device__ __forceinline__ void fma2(f32x2& d, f32x2 a, f32x2 b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ f32x2 widen(uint32_t w) { return pack2(bf16lo(w), bf16hi(w)); }
 
 __global__ void __launch_bounds__(256) count_kernel(const BwdParams p) {
   const int lane = threadIdx.x & 31;
@@ -152,22 +172,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
   const int n_rows = *p.n_ell;
   for (int i = blockIdx.x * kWarps + wid; i < n_rows; i += warps_total) {
     const int t = p.ell_rows[i];
-    float dyf[NC][8];
-    float acc[NC][8];
+    f32x2 dyf[NC][4];  // dy_t, fp32 pairs
+    f32x2 acc[NC][4];  // dx_t accumulator, fp32 pairs
     const float* dyr = p.dy + static_cast<size_t>(t) * D;
 #pragma unroll
     for (int q = 0; q < NC; ++q) {
       if (own(q)) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(dyr + 8 * (lane + 32 * q)));
         const float4 b = __ldg(reinterpret_cast<const float4*>(dyr + 8 * (lane + 32 * q)) + 1);
-        dyf[q][0] = a.x; dyf[q][1] = a.y; dyf[q][2] = a.z; dyf[q][3] = a.w;
-        dyf[q][4] = b.x; dyf[q][5] = b.y; dyf[q][6] = b.z; dyf[q][7] = b.w;
+        dyf[q][0] = pack2(a.x, a.y);
+        dyf[q][1] = pack2(a.z, a.w);
+        dyf[q][2] = pack2(b.x, b.y);
+        dyf[q][3] = pack2(b.z, b.w);
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dyf[q][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) dyf[q][e] = 0ull;
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[q][e] = 0.0f;
+      for (int e = 0; e < 4; ++e) acc[q][e] = 0ull;
     }
 
     const size_t rt0 = static_cast<size_t>(i) * p.n_t;
@@ -209,25 +231,29 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
                                                                         stage_bytes);
           const uint4* sg = sd + nch;
           const uint4* su = sg + nch;
-          float pp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          f32x2 pp[4] = {0ull, 0ull, 0ull, 0ull};  // eight independent partial sums
 #pragma unroll
           for (int q = 0; q < NC; ++q) {
             if (own(q)) {
               const uint4 a = sd[lane + 32 * q];
               const uint32_t a4[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-              for (int r = 0; r < 4; ++r) {
-                pp[r] = fmaf(dyf[q][2 * r], bf16lo(a4[r]), pp[r]);
-                pp[r] = fmaf(dyf[q][2 * r + 1], bf16hi(a4[r]), pp[r]);
-              }
+              for (int r = 0; r < 4; ++r) fma2(pp[r], dyf[q][r], widen(a4[r]));
             }
           }
-          float da = (pp[0] + pp[1]) + (pp[2] + pp[3]);
+          float p0, p1, p2, p3, p4, p5, p6, p7;
+          unpack2(pp[0], p0, p1);
+          unpack2(pp[1], p2, p3);
+          unpack2(pp[2], p4, p5);
+          unpack2(pp[3], p6, p7);
+          float da = ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
           const float u = p.u_ell[en.pos];
           const float du = da * en.h;
           const float dz = fmaf(da, u, p.lambda);
+          const f32x2 dz2 = pack2(dz, dz);
+          const f32x2 du2 = pack2(du, du);
 #pragma unroll
           for (int q = 0; q < NC; ++q) {
             if (own(q)) {
@@ -237,10 +263,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
               const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
               for (int r = 0; r < 4; ++r) {
-                acc[q][2 * r] = fmaf(dz, bf16lo(g4[r]), acc[q][2 * r]);
-                acc[q][2 * r + 1] = fmaf(dz, bf16hi(g4[r]), acc[q][2 * r + 1]);
-                acc[q][2 * r] = fmaf(du, bf16lo(w4[r]), acc[q][2 * r]);
-                acc[q][2 * r + 1] = fmaf(du, bf16hi(w4[r]), acc[q][2 * r + 1]);
+                fma2(acc[q][r], dz2, widen(g4[r]));
+                fma2(acc[q][r], du2, widen(w4[r]));
               }
             }
           }
@@ -262,9 +286,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
 #pragma unroll
     for (int q = 0; q < NC; ++q) {
       if (own(q)) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) unpack2(acc[q][e], v[2 * e], v[2 * e + 1]);
         float4* o = reinterpret_cast<float4*>(dxr + 8 * (lane + 32 * q));
-        o[0] = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-        o[1] = make_float4(acc[q][4], acc[q][5], acc[q][6], acc[q][7]);
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
       }
     }
   }
@@ -341,7 +368,8 @@ template <int NC>
 twell_status launch_ell_bwd(BwdParams p, const DeviceInfo& dev, cudaStream_t s) {
   const int stage_bytes = 6 * p.D;
   const int fixed = kMaxStages * 8 + kListCap * static_cast<int>(sizeof(BEntry));
-  int P = (kSmemBudget / kWarps - fixed) / stage_bytes;
+  const int budget = kSmemBudget < dev.max_smem_optin ? kSmemBudget : dev.max_smem_optin;
+  int P = (budget / kWarps - fixed) / stage_bytes;
   if (P > kMaxStages) P = kMaxStages;
   if (P < 1) return TWELL_ERR_UNSUPPORTED;
   p.stages = P;
