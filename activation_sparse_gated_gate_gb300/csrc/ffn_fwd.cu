@@ -176,9 +176,25 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
             const size_t so = (row_rt + k) * static_cast<size_t>(p.W);
             const int s0 = max(0, base - off);
             const int s1 = min(n, base + kListCap - off);
-            for (int s = s0; s < s1; ++s)
-              list[off + s - base] =
-                  Entry{jbase + p.col[so + s], p.val[so + s], static_cast<int32_t>(so + s)};
+            if ((p.W & 3) == 0) {
+              // four slots per 16-byte load (slots past the count are read, not used)
+              for (int q = s0 & ~3; q < s1; q += 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(p.val + so + q));
+                const uint32_t c4 = __ldg(reinterpret_cast<const uint32_t*>(p.col + so + q));
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int s = q + e;
+                  if (s >= s0 && s < s1)
+                    list[off + s - base] = Entry{jbase + static_cast<int>((c4 >> (8 * e)) & 0xffu),
+                                                 vv[e], static_cast<int32_t>(so + s)};
+                }
+              }
+            } else {
+              for (int s = s0; s < s1; ++s)
+                list[off + s - base] =
+                    Entry{jbase + p.col[so + s], p.val[so + s], static_cast<int32_t>(so + s)};
+            }
           } else {
             const float* sl = p.spill_val + static_cast<size_t>(spill) * TWELL_TILE;
             int e = off;
