@@ -4,11 +4,12 @@
 // products only for the nonzero elements and keeping DRAM traffic low).
 //
 // Work unit = (token row t, range of G column tiles); one warp per unit at a
-// time (12 warps per CTA for D <= 2304, else 8; one CTA per SM; units
-// strided over the grid).  With
+// time (12 warps per CTA for D <= 2304, else 8; one CTA per SM).  With
 // many tokens G covers the whole row and the warp stores y_t; with few
 // tokens (decode) rows are split into several units so every SM gets work,
 // and each unit adds its partial y_t with 16-byte atomics into a zeroed y.
+// Each CTA takes a contiguous range of units and hands them to its warps in
+// order of completion.
 // x_t (bf16 pairs) and the fp32 accumulator of y_t live in registers, spread
 // over the 32 lanes in 8-element chunks (lane l holds chunks l, l+32, ...).
 //
@@ -110,11 +111,21 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
     ptx::bulk_load(dst + row_bytes, p.Wd + static_cast<size_t>(e.j) * D, row_bytes, &bars[s]);
   };
 
-  const int warps_total = gridDim.x * kWarps;
+  // Each CTA owns a contiguous range of units; its warps take the next unit
+  // of the range from a shared counter as they finish the previous one, so a
+  // few heavy rows delay one warp by one row rather than a fixed share.
+  __shared__ int next_unit;
   const long long units =
       ELL ? static_cast<long long>(*p.n_rows) : static_cast<long long>(p.T) * p.upr;
-  for (long long u = static_cast<long long>(blockIdx.x) * kWarps + wid; u < units;
-       u += warps_total) {
+  const long long u_begin = units * blockIdx.x / gridDim.x;
+  const long long u_end = units * (blockIdx.x + 1) / gridDim.x;
+  if (threadIdx.x == 0) next_unit = 0;
+  __syncthreads();
+  for (;;) {
+    int take = 0;
+    if (lane == 0) take = atomicAdd(&next_unit, 1);
+    const long long u = u_begin + __shfl_sync(0xffffffffu, take, 0);
+    if (u >= u_end) break;
     // row: index into the count / slot arrays; t: token (x and y row)
     const int row = ELL ? static_cast<int>(u) : static_cast<int>(u / p.upr);
     const int t = ELL ? p.ell_rows[row] : row;

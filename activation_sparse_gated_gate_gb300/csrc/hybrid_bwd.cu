@@ -168,9 +168,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
     ptx::bulk_load(dst + 2 * row_bytes, p.Wu_t + off, row_bytes, &bars[s]);
   };
 
-  const int warps_total = gridDim.x * kWarps;
+  // contiguous row range per CTA, handed to its warps in order of completion
+  __shared__ int next_row;
   const int n_rows = *p.n_ell;
-  for (int i = blockIdx.x * kWarps + wid; i < n_rows; i += warps_total) {
+  const int i_begin = static_cast<int>(static_cast<long long>(n_rows) * blockIdx.x / gridDim.x);
+  const int i_end =
+      static_cast<int>(static_cast<long long>(n_rows) * (blockIdx.x + 1) / gridDim.x);
+  if (threadIdx.x == 0) next_row = 0;
+  __syncthreads();
+  for (;;) {
+    int take = 0;
+    if (lane == 0) take = atomicAdd(&next_row, 1);
+    const int i = i_begin + __shfl_sync(0xffffffffu, take, 0);
+    if (i >= i_end) break;
     const int t = p.ell_rows[i];
     f32x2 dyf[NC][4];  // dy_t, fp32 pairs
     f32x2 acc[NC][4];  // dx_t accumulator, fp32 pairs
