@@ -76,6 +76,11 @@ _SIGNATURES = {
     "hybrid_ffn_bwd": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_ptr, c_ptr,
                                c_ptr, c_i32, c_ptr, ctypes.c_float, c_ptr, c_ptr, c_ptr, c_ptr,
                                c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "hybrid_ffn_fwd_tc": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_i32,
+                                  c_ptr, c_ptr, c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "hybrid_ffn_bwd_tc": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_ptr,
+                                  c_ptr, c_ptr, c_i32, c_ptr, ctypes.c_float, c_ptr, c_ptr, c_ptr,
+                                  c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "hybrid_ffn_fwd_noalloc": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_i32,
                                        c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "twell_status_string": (ctypes.c_char_p, [c_i32]),
@@ -248,6 +253,8 @@ def twell_to_hybrid(h: TwELL, out: Hybrid, status=None, stream=None):
 
 WS_HYBRID_FWD = 1
 WS_HYBRID_BWD = 2
+WS_HYBRID_FWD_TC = 3
+WS_HYBRID_BWD_TC = 4
 
 
 def twell_workspace_size(op: int, T: int, D: int, F: int, cap: int, max_dense: int) -> int:
@@ -262,6 +269,19 @@ def _workspace(nbytes, device):
 def hybrid_ffn_fwd(x, h: Hybrid, Wu_t, Wd, y=None, u_ell=None, U_dense=None, ws=None,
                    status=None, stream=None):
     """Hybrid training forward; returns (y, u_ell, U_dense)."""
+    return _hybrid_fwd("hybrid_ffn_fwd", WS_HYBRID_FWD, x, h, Wu_t, Wd, y, u_ell, U_dense, ws,
+                       status, stream)
+
+
+def hybrid_ffn_fwd_tc(x, h: Hybrid, Wu_t, Wd, y=None, u_ell=None, U_dense=None, ws=None,
+                      status=None, stream=None):
+    """Hybrid training forward, ELL rows on the tensor cores; returns
+    (y, u_ell, U_dense)."""
+    return _hybrid_fwd("hybrid_ffn_fwd_tc", WS_HYBRID_FWD_TC, x, h, Wu_t, Wd, y, u_ell, U_dense,
+                       ws, status, stream)
+
+
+def _hybrid_fwd(name, op, x, h, Wu_t, Wd, y, u_ell, U_dense, ws, status, stream):
     _need(x, torch.bfloat16, "x")
     _need(Wu_t, torch.bfloat16, "Wu_t")
     _need(Wd, torch.bfloat16, "Wd")
@@ -273,21 +293,35 @@ def hybrid_ffn_fwd(x, h: Hybrid, Wu_t, Wd, y=None, u_ell=None, U_dense=None, ws=
         u_ell = torch.empty((T, h.n_t, h.cap), dtype=torch.float32, device=dev)
     if U_dense is None:
         U_dense = torch.empty((max(h.max_dense, 1), h.F), dtype=torch.float32, device=dev)
-    need = twell_workspace_size(WS_HYBRID_FWD, T, D, h.F, h.cap, h.max_dense)
+    need = twell_workspace_size(op, T, D, h.F, h.cap, h.max_dense)
     if ws is None:
         ws = _workspace(need, dev)
     status = h.status if status is None else status
     with torch.cuda.device(dev):
-        _check(lib().hybrid_ffn_fwd(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
+        _check(getattr(lib(), name)(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
                                     _ptr(y), _ptr(u_ell), _ptr(U_dense), _ptr(ws),
                                     ws.numel(), _ptr(status), _stream(stream)),
-               "hybrid_ffn_fwd")
+               name)
     return y, u_ell, U_dense
 
 
 def hybrid_ffn_bwd(x, h: Hybrid, u_ell, U_dense, Wg_t, Wu_t, Wd, dy, l1_coeff, dx=None,
                    dWg_t=None, dWu_t=None, dWd=None, ws=None, status=None, stream=None):
     """Hybrid training backward with the L1 term; returns (dx, dWg_t, dWu_t, dWd)."""
+    return _hybrid_bwd("hybrid_ffn_bwd", WS_HYBRID_BWD, x, h, u_ell, U_dense, Wg_t, Wu_t, Wd, dy,
+                       l1_coeff, dx, dWg_t, dWu_t, dWd, ws, status, stream)
+
+
+def hybrid_ffn_bwd_tc(x, h: Hybrid, u_ell, U_dense, Wg_t, Wu_t, Wd, dy, l1_coeff, dx=None,
+                      dWg_t=None, dWu_t=None, dWd=None, ws=None, status=None, stream=None):
+    """Hybrid training backward, ELL rows on the tensor cores; returns
+    (dx, dWg_t, dWu_t, dWd)."""
+    return _hybrid_bwd("hybrid_ffn_bwd_tc", WS_HYBRID_BWD_TC, x, h, u_ell, U_dense, Wg_t, Wu_t,
+                       Wd, dy, l1_coeff, dx, dWg_t, dWu_t, dWd, ws, status, stream)
+
+
+def _hybrid_bwd(name, op, x, h, u_ell, U_dense, Wg_t, Wu_t, Wd, dy, l1_coeff, dx, dWg_t, dWu_t,
+                dWd, ws, status, stream):
     for t, n in ((x, "x"), (Wg_t, "Wg_t"), (Wu_t, "Wu_t"), (Wd, "Wd")):
         _need(t, torch.bfloat16, n)
     _need(dy, torch.float32, "dy")
@@ -299,17 +333,17 @@ def hybrid_ffn_bwd(x, h: Hybrid, u_ell, U_dense, Wg_t, Wu_t, Wd, dy, l1_coeff, d
     dWg_t = torch.empty((F, D), dtype=f32, device=dev) if dWg_t is None else dWg_t
     dWu_t = torch.empty((F, D), dtype=f32, device=dev) if dWu_t is None else dWu_t
     dWd = torch.empty((F, D), dtype=f32, device=dev) if dWd is None else dWd
-    need = twell_workspace_size(WS_HYBRID_BWD, T, D, F, h.cap, h.max_dense)
+    need = twell_workspace_size(op, T, D, F, h.cap, h.max_dense)
     if ws is None:
         ws = _workspace(need, dev)
     status = h.status if status is None else status
     with torch.cuda.device(dev):
-        _check(lib().hybrid_ffn_bwd(_ptr(x), ctypes.byref(h.struct), _ptr(u_ell), _ptr(U_dense),
+        _check(getattr(lib(), name)(_ptr(x), ctypes.byref(h.struct), _ptr(u_ell), _ptr(U_dense),
                                     _ptr(Wg_t), _ptr(Wu_t), _ptr(Wd), D, _ptr(dy),
                                     float(l1_coeff), _ptr(dx), _ptr(dWg_t), _ptr(dWu_t),
                                     _ptr(dWd), _ptr(ws), ws.numel(), _ptr(status),
                                     _stream(stream)),
-               "hybrid_ffn_bwd")
+               name)
     return dx, dWg_t, dWu_t, dWd
 
 

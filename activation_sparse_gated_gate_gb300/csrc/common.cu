@@ -67,6 +67,14 @@ twell_status check_twell(const twell_t* h, int32_t T, int32_t F, bool need_spill
 twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
                                uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                                uint64_t pitch) {
+  return make_tmap_2d(map, 2, base, inner, outer, box_inner, box_outer,
+                      (pitch ? pitch : inner) * 2, true);
+}
+
+twell_status make_tmap_2d(CUtensorMap* map, int elem_bytes, const void* base, uint64_t inner,
+                          uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                          uint64_t pitch_bytes, bool swizzle128) {
+  if (elem_bytes != 1 && elem_bytes != 2) return TWELL_ERR_INVALID;
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -77,13 +85,14 @@ twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
   });
   if (!g_encode) return TWELL_ERR_CUDA;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {(pitch ? pitch : inner) * 2};
+  cuuint64_t strides[1] = {pitch_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(
+      map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TWELL_OK : TWELL_ERR_INVALID;
 }
 

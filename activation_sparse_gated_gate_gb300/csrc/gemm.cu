@@ -100,15 +100,41 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int m, int n0,
     float* uo = p.U_out + off;
     uint16_t* hi = p.S_out + static_cast<int64_t>(m) * p.lds + n0;
     uint16_t* lo = hi + N;
+    if (full && (N & 7) == 0 && (p.lds & 7) == 0) {  // 16-byte vectors (row offsets stay 32-byte aligned)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (full || n0 + i < N) {
-        const float u = __uint_as_float(r[i]);
-        uo[i] = u;
-        uint16_t a_hi, a_lo;
-        split(h[i] * u, a_hi, a_lo);
-        hi[i] = a_hi;
-        lo[i] = a_lo;
+      for (int g = 0; g < 4; ++g) {
+        const float4 h0 = reinterpret_cast<const float4*>(h)[2 * g];
+        const float4 h1 = reinterpret_cast<const float4*>(h)[2 * g + 1];
+        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint16_t h_a, l_a, h_b, l_b;
+          split(hv[2 * e] * __uint_as_float(r[8 * g + 2 * e]), h_a, l_a);
+          split(hv[2 * e + 1] * __uint_as_float(r[8 * g + 2 * e + 1]), h_b, l_b);
+          wh[e] = h_a | (static_cast<uint32_t>(h_b) << 16);
+          wl[e] = l_a | (static_cast<uint32_t>(l_b) << 16);
+        }
+        reinterpret_cast<float4*>(uo)[2 * g] =
+            make_float4(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]),
+                        __uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
+        reinterpret_cast<float4*>(uo)[2 * g + 1] =
+            make_float4(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]),
+                        __uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
+        reinterpret_cast<uint4*>(hi)[g] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        reinterpret_cast<uint4*>(lo)[g] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (full || n0 + i < N) {
+          const float u = __uint_as_float(r[i]);
+          uo[i] = u;
+          uint16_t a_hi, a_lo;
+          split(h[i] * u, a_hi, a_lo);
+          hi[i] = a_hi;
+          lo[i] = a_lo;
+        }
       }
     }
   } else {  // EPI_DA
@@ -116,20 +142,45 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int m, int n0,
     const float* h = p.H + off;
     const float* u = p.U_in + off;
     uint16_t* s = p.S_out + static_cast<int64_t>(m) * p.lds + n0;
+    auto da_at = [&](int i, float hv, float uv, uint16_t& zh, uint16_t& zl, uint16_t& wh,
+                     uint16_t& wl) {
+      const float da = __uint_as_float(r[i]);
+      split(hv > 0.0f ? fmaf(da, uv, p.lambda) : 0.0f, zh, zl);
+      split(da * hv, wh, wl);
+    };
+    if (full && (N & 7) == 0 && (p.lds & 7) == 0) {  // 16-byte vectors
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (full || n0 + i < N) {
-        const float da = __uint_as_float(r[i]);
-        const float hv = h[i];
-        const float dz = hv > 0.0f ? fmaf(da, u[i], p.lambda) : 0.0f;
-        const float du = da * hv;
-        uint16_t a, b;
-        split(dz, a, b);
-        s[i] = a;
-        s[i + N] = b;
-        split(du, a, b);
-        s[i + 2 * N] = a;
-        s[i + 3 * N] = b;
+      for (int g = 0; g < 4; ++g) {
+        const float4 h0 = reinterpret_cast<const float4*>(h)[2 * g];
+        const float4 h1 = reinterpret_cast<const float4*>(h)[2 * g + 1];
+        const float4 u0 = reinterpret_cast<const float4*>(u)[2 * g];
+        const float4 u1 = reinterpret_cast<const float4*>(u)[2 * g + 1];
+        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t w[4][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint16_t a[4], b[4];
+          da_at(8 * g + 2 * e, hv[2 * e], uv[2 * e], a[0], a[1], a[2], a[3]);
+          da_at(8 * g + 2 * e + 1, hv[2 * e + 1], uv[2 * e + 1], b[0], b[1], b[2], b[3]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w[q][e] = a[q] | (static_cast<uint32_t>(b[q]) << 16);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          reinterpret_cast<uint4*>(s + q * N)[g] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (full || n0 + i < N) {
+          uint16_t zh, zl, wh, wl;
+          da_at(i, h[i], u[i], zh, zl, wh, wl);
+          s[i] = zh;
+          s[i + N] = zl;
+          s[i + 2 * N] = wh;
+          s[i + 3 * N] = wl;
+        }
       }
     }
   }
@@ -404,14 +455,37 @@ __global__ void __launch_bounds__(256) transpose_kernel(const TransposeArgs a) {
 template <int MODE>
 __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
   const int R_act = a.R_dyn ? min(a.R, *a.R_dyn) : a.R;
-  const int per_row = MODE == 0 ? a.C / 8 : a.C / 4;
-  const long long total = static_cast<long long>(R_act) * per_row;
+  const int R_out = a.pad > 0 ? min(a.R, (R_act + a.pad - 1) / a.pad * a.pad) : R_act;
+  const int per_row = MODE == 1 ? a.C / 4 : a.C / 8;
+  const long long total = static_cast<long long>(R_out) * per_row;
   for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
        v += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int i = static_cast<int>(v / per_row);
     const int q = static_cast<int>(v % per_row);
+    if (i >= R_act) {  // zero padding rows
+      if (MODE == 1) {
+        uint16_t* o = a.out + static_cast<int64_t>(i) * a.ldo + 4 * q;
+        reinterpret_cast<uint2*>(o)[0] = make_uint2(0u, 0u);
+        reinterpret_cast<uint2*>(o + a.C)[0] = make_uint2(0u, 0u);
+      } else {
+        reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(i) * a.ldo)[q] =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
     const int64_t sr = a.row_idx ? a.row_idx[i] : i;
-    if (MODE == 0) {
+    if (MODE == 2) {
+      const float4* s =
+          reinterpret_cast<const float4*>(static_cast<const float*>(a.src) + sr * a.lds) + 2 * q;
+      const float4 x0 = s[0], x1 = s[1];
+      const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = bf16_bits(f[2 * e]) | (static_cast<uint32_t>(bf16_bits(f[2 * e + 1])) << 16);
+      reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(i) * a.ldo)[q] =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (MODE == 0) {
       const uint4 x = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) +
                                                      sr * a.lds)[q];
       reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(i) * a.ldo)[q] = x;
@@ -491,14 +565,18 @@ twell_status transpose_run(int mode, const TransposeArgs& a, cudaStream_t s) {
 
 twell_status gather_run(int mode, const GatherArgs& a, cudaStream_t s) {
   if (a.R <= 0) return TWELL_OK;
-  const long long per_row = mode == 0 ? a.C / 8 : a.C / 4;
+  const long long per_row = mode == 1 ? a.C / 4 : a.C / 8;
   long long blocks = (static_cast<long long>(a.R) * per_row + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
   if (mode == 0)
     gather_kernel<0><<<static_cast<int>(blocks), 256, 0, s>>>(a);
-  else
+  else if (mode == 1)
     gather_kernel<1><<<static_cast<int>(blocks), 256, 0, s>>>(a);
+  else if (mode == 2)
+    gather_kernel<2><<<static_cast<int>(blocks), 256, 0, s>>>(a);
+  else
+    return TWELL_ERR_INVALID;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

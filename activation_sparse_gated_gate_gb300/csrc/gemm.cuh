@@ -95,9 +95,12 @@ struct TransposeArgs {
 };
 twell_status transpose_run(int mode, const TransposeArgs& a, cudaStream_t s);
 
-// out[i][:] = src[row_idx[i]][:] for i < min(R, *R_dyn):
+// out[i][:] = src[row_idx[i]][:] for i < R_act = min(R, *R_dyn):
 //   MODE 0  bf16 rows of C elements (C % 8 == 0), out pitch ldo
 //   MODE 1  fp32 rows split into bf16 [hi (C) | lo (C)], out pitch ldo
+//   MODE 2  fp32 rows rounded to bf16 (C % 8 == 0), out pitch ldo
+// With pad > 0, rows R_act <= i < min(R, R_act rounded up to pad) are
+// written as zeros.
 struct GatherArgs {
   const void* src;
   int64_t lds;
@@ -106,6 +109,7 @@ struct GatherArgs {
   const int32_t* R_dyn;
   uint16_t* out;
   int64_t ldo;
+  int32_t pad;
 };
 twell_status gather_run(int mode, const GatherArgs& a, cudaStream_t s);
 

@@ -8,6 +8,8 @@ namespace twell {
 
 struct WsLayout {
   size_t bytes = 0;
+  // tensor-core ELL path: gathered bf16 x / dy rows, bf16 ELL values
+  size_t xe = 0, dye = 0, ae = 0, dze = 0, dzl = 0, due = 0;
   // forward
   size_t xo = 0, wdT = 0, asplit = 0;
   // backward
@@ -37,15 +39,27 @@ inline WsLayout ws_layout(int op, int64_t T, int64_t D, int64_t F, int64_t cap,
   size_t cur = 0;
   const int64_t n_t = F / TWELL_TILE;
   w.mpad = (max_dense + 63) / 64 * 64;
-  if (op == 1) {
+  if (op == 3 || op == 4) {
+    w.xe = ws_take(&cur, T * D * 2);
+    w.ae = ws_take(&cur, T * n_t * cap * 2);
+  }
+  if (op == 4) {
+    w.dye = ws_take(&cur, T * 2 * D * 2);  // bf16 [hi | lo] rows
+    w.dze = ws_take(&cur, T * n_t * cap * 2);
+    w.dzl = ws_take(&cur, T * n_t * cap * 2);
+    w.due = ws_take(&cur, T * n_t * cap * 2);
+  }
+  if (op == 1 || op == 3) {
     w.xo = ws_take(&cur, max_dense * D * 2);
     w.wdT = ws_take(&cur, D * F * 2);
     w.asplit = ws_take(&cur, max_dense * 2 * F * 2);
-  } else if (op == 2) {
-    w.cnt = ws_take(&cur, F * 4);
-    w.offs = ws_take(&cur, (F + 1) * 4);
-    w.cursor = ws_take(&cur, F * 4);
-    w.records = ws_take(&cur, T * n_t * cap * sizeof(BwdRecord));
+  } else if (op == 2 || op == 4) {
+    if (op == 2) {
+      w.cnt = ws_take(&cur, F * 4);
+      w.offs = ws_take(&cur, (F + 1) * 4);
+      w.cursor = ws_take(&cur, F * 4);
+      w.records = ws_take(&cur, T * n_t * cap * sizeof(BwdRecord));
+    }
     w.xo = ws_take(&cur, max_dense * D * 2);
     w.dys = ws_take(&cur, max_dense * 2 * D * 2);
     w.g = ws_take(&cur, max_dense * 4 * F * 2);
@@ -64,5 +78,18 @@ inline WsLayout ws_layout(int op, int64_t T, int64_t D, int64_t F, int64_t cap,
   w.bytes = (cur + 255) & ~static_cast<size_t>(255);
   return w;
 }
+
+// Dense overflow rows of the hybrid forward / backward (tensor cores with
+// bf16 hi/lo operand splits), shared by the CUDA-core and tensor-core entry
+// points; `w` is the workspace laid out by L.
+twell_status dense_rows_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
+                            const uint16_t* Wd, int32_t D, float* y, float* U_dense,
+                            uint8_t* w, const WsLayout& L, int32_t* status_dev,
+                            const DeviceInfo& dev, cudaStream_t s);
+twell_status dense_rows_bwd(const uint16_t* x, const hybrid_t* h, const float* U_dense,
+                            const uint16_t* Wg_t, const uint16_t* Wu_t, const uint16_t* Wd,
+                            int32_t D, const float* dy, float l1_coeff, float* dx, float* dWg_t,
+                            float* dWu_t, float* dWd, uint8_t* w, const WsLayout& L,
+                            int32_t* status_dev, const DeviceInfo& dev, cudaStream_t s);
 
 }  // namespace twell

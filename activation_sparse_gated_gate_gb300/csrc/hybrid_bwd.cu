@@ -501,6 +501,19 @@ extern "C" twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, con
   if (h->max_dense == 0) return TWELL_OK;
 
   // ---- dense overflow rows
+  return dense_rows_bwd(x, h, U_dense, Wg_t, Wu_t, Wd, D, dy, l1_coeff, dx, dWg_t, dWu_t, dWd,
+                        w, L, status_dev, dev, s);
+}
+
+namespace twell {
+
+twell_status dense_rows_bwd(const uint16_t* x, const hybrid_t* h, const float* U_dense,
+                            const uint16_t* Wg_t, const uint16_t* Wu_t, const uint16_t* Wd,
+                            int32_t D, const float* dy, float l1_coeff, float* dx, float* dWg_t,
+                            float* dWu_t, float* dWd, uint8_t* w, const WsLayout& L,
+                            int32_t* status_dev, const DeviceInfo& dev, cudaStream_t s) {
+  const int32_t F = h->F;
+  twell_status st;
   const int32_t MD = h->max_dense;
   const int64_t mp = L.mpad;
   uint16_t* Xo = reinterpret_cast<uint16_t*>(w + L.xo);
@@ -672,3 +685,5 @@ extern "C" twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, con
   }
   return TWELL_OK;
 }
+
+}  // namespace twell

@@ -16,55 +16,18 @@
 
 extern "C" size_t twell_workspace_size(int32_t op, int32_t T, int32_t D, int32_t F,
                                        int32_t cap, int32_t max_dense) {
-  if ((op != 1 && op != 2) || T < 0 || D <= 0 || F <= 0 || cap < 1 || max_dense < 0) return 0;
+  if (op < 1 || op > 4 || T < 0 || D <= 0 || F <= 0 || cap < 1 || max_dense < 0) return 0;
   return twell::ws_layout(op, T, D, F, cap, max_dense).bytes;
 }
 
-extern "C" twell_status hybrid_ffn_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
-                                       const uint16_t* Wd, int32_t D, float* y, float* u_ell,
-                                       float* U_dense, void* ws, size_t ws_bytes,
-                                       int32_t* status_dev, void* stream) {
-  using namespace twell;
-  if (h == nullptr) return TWELL_ERR_INVALID;
-  const int32_t T = h->T, F = h->F;
-  if (T < 0 || F <= 0 || F % TWELL_TILE != 0 || D <= 0 || D % 8 != 0) return TWELL_ERR_INVALID;
-  twell_status st = check_hybrid(h, T, F);
-  if (st != TWELL_OK) return st;
-  if (T == 0) return TWELL_OK;
-  const WsLayout L = ws_layout(1, T, D, F, h->cap, h->max_dense);
-  if (!x || !Wu_t || !Wd || !y || !u_ell || !status_dev) return TWELL_ERR_INVALID;
-  if (h->max_dense > 0 && (!U_dense || !ws || ws_bytes < L.bytes)) return TWELL_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y) ||
-      !aligned16(u_ell) || (U_dense && !aligned16(U_dense)) ||
-      (reinterpret_cast<uintptr_t>(ws) & 255u))
-    return TWELL_ERR_INVALID;
-  if (D > 256 * 12) return TWELL_ERR_UNSUPPORTED;
-  DeviceInfo dev;
-  if ((st = require_sm103(&dev)) != TWELL_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+namespace twell {
 
-  // ELL rows
-  FfnParams p{};
-  p.x = x;
-  p.Wu_t = Wu_t;
-  p.Wd = Wd;
-  p.y = y;
-  p.val = h->ell_val;
-  p.col = h->ell_col;
-  p.cnt = h->ell_cnt;
-  p.T = T;
-  p.D = D;
-  p.n_t = F / TWELL_TILE;
-  p.W = h->cap;
-  p.status = status_dev;
-  p.n_rows = h->n_ell;
-  p.ell_rows = h->ell_rows;
-  p.u_save = u_ell;
-  if ((st = launch_fused(p, dev, s, true)) != TWELL_OK) return st;
-  if (h->max_dense == 0) return TWELL_OK;
-
-  // dense overflow rows
-  uint8_t* w = static_cast<uint8_t*>(ws);
+twell_status dense_rows_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
+                            const uint16_t* Wd, int32_t D, float* y, float* U_dense,
+                            uint8_t* w, const WsLayout& L, int32_t* status_dev,
+                            const DeviceInfo& dev, cudaStream_t s) {
+  const int32_t F = h->F;
+  twell_status st;
   uint16_t* Xo = reinterpret_cast<uint16_t*>(w + L.xo);
   uint16_t* WdT = reinterpret_cast<uint16_t*>(w + L.wdT);
   uint16_t* As = reinterpret_cast<uint16_t*>(w + L.asplit);
@@ -142,4 +105,54 @@ extern "C" twell_status hybrid_ffn_fwd(const uint16_t* x, const hybrid_t* h, con
     if ((st = gemm_run(maps, a, wide, dev, s)) != TWELL_OK) return st;
   }
   return TWELL_OK;
+}
+
+}  // namespace twell
+
+extern "C" twell_status hybrid_ffn_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
+                                       const uint16_t* Wd, int32_t D, float* y, float* u_ell,
+                                       float* U_dense, void* ws, size_t ws_bytes,
+                                       int32_t* status_dev, void* stream) {
+  using namespace twell;
+  if (h == nullptr) return TWELL_ERR_INVALID;
+  const int32_t T = h->T, F = h->F;
+  if (T < 0 || F <= 0 || F % TWELL_TILE != 0 || D <= 0 || D % 8 != 0) return TWELL_ERR_INVALID;
+  twell_status st = check_hybrid(h, T, F);
+  if (st != TWELL_OK) return st;
+  if (T == 0) return TWELL_OK;
+  const WsLayout L = ws_layout(1, T, D, F, h->cap, h->max_dense);
+  if (!x || !Wu_t || !Wd || !y || !u_ell || !status_dev) return TWELL_ERR_INVALID;
+  if (h->max_dense > 0 && (!U_dense || !ws || ws_bytes < L.bytes)) return TWELL_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y) ||
+      !aligned16(u_ell) || (U_dense && !aligned16(U_dense)) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return TWELL_ERR_INVALID;
+  if (D > 256 * 12) return TWELL_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if ((st = require_sm103(&dev)) != TWELL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // ELL rows
+  FfnParams p{};
+  p.x = x;
+  p.Wu_t = Wu_t;
+  p.Wd = Wd;
+  p.y = y;
+  p.val = h->ell_val;
+  p.col = h->ell_col;
+  p.cnt = h->ell_cnt;
+  p.T = T;
+  p.D = D;
+  p.n_t = F / TWELL_TILE;
+  p.W = h->cap;
+  p.status = status_dev;
+  p.n_rows = h->n_ell;
+  p.ell_rows = h->ell_rows;
+  p.u_save = u_ell;
+  if ((st = launch_fused(p, dev, s, true)) != TWELL_OK) return st;
+  if (h->max_dense == 0) return TWELL_OK;
+
+  // dense overflow rows
+  return dense_rows_fwd(x, h, Wu_t, Wd, D, y, U_dense, static_cast<uint8_t*>(ws), L,
+                        status_dev, dev, s);
 }

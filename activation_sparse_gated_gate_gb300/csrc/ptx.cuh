@@ -184,14 +184,56 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B (both
-// K-major) and an fp32 accumulator of shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor of an MN-major operand tile with 128-byte
+// swizzling: atoms of 64 bf16 along M/N (128 bytes) x 8 rows along K, the
+// K rows of an atom 128 bytes apart.  Atoms follow each other along M/N
+// every `lbo` bytes (leading byte offset) and along K every `sbo` bytes
+// (stride byte offset; 1024 when an atom column is stacked contiguously).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t lbo,
+                                                        uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B and an
+// fp32 accumulator of shape M x N.  A and B are K-major unless a_mn / b_mn
+// (bits 15 / 16: the operand is stored M-major / N-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
+                                                      bool b_mn = false) {
   return (1u << 4)                                  // D format: f32
          | (1u << 7)                                // A format: bf16
          | (1u << 10)                               // B format: bf16
+         | (a_mn ? 1u << 15 : 0u)                   // A major-ness
+         | (b_mn ? 1u << 16 : 0u)                   // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier `id` over `count` threads that also returns whether any
+// participating thread passed `pred` true.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.u32 p, %3, 0;\n"
+      "bar.red.or.pred q, %1, %2, p;\n"
+      "selp.u32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
 }
 
 }  // namespace ptx

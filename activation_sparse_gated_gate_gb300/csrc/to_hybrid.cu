@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
     p.ell_cnt[dst_rt + k] = static_cast<uint8_t>(c);
     float* dv = p.ell_val + (dst_rt + k) * p.C;
     uint8_t* dc = p.ell_col + (dst_rt + k) * p.C;
+    for (int s = c; s < p.C; ++s) dc[s] = 0xffu;  // padding slots: column sentinel
     if (c <= p.W) {
       const float* sv = p.val + (src_rt + k) * p.W;
       const uint8_t* sc = p.col + (src_rt + k) * p.W;

@@ -150,7 +150,8 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
  *   row_map[t]                i >= 0: ELL row i;  i < 0: dense row -(i+1)
  *   ell_rows[i]               token of ELL row i, i < n_ell
  *   ell_cnt[i*n_t + k]        count of ELL row i in tile k (<= C)
- *   ell_col/ell_val[(i*n_t + k)*C + s]   its entries, ascending, s < count
+ *   ell_col/ell_val[(i*n_t + k)*C + s]   its entries, ascending, s < count;
+ *                             padding slots (s >= count) hold column 0xFF
  *   dense_rows[i]             token of dense row i, i < min(n_dense, max_dense)
  *   dense_h[i*F + j]          fp32 ReLU(z) of that token (zeros where inactive)
  * Sizes: row_map, ell_rows [T] int32; ell_cnt [T][n_t] uint8;
@@ -186,7 +187,12 @@ twell_status twell_to_hybrid(const twell_t* h, const hybrid_t* out, int32_t* sta
                              void* stream);
 
 /* Workspace operations for twell_workspace_size. */
-enum { TWELL_WS_HYBRID_FWD = 1, TWELL_WS_HYBRID_BWD = 2 };
+enum {
+  TWELL_WS_HYBRID_FWD = 1,
+  TWELL_WS_HYBRID_BWD = 2,
+  TWELL_WS_HYBRID_FWD_TC = 3,
+  TWELL_WS_HYBRID_BWD_TC = 4
+};
 
 /*
  * Bytes of device workspace `op` needs for a hybrid of T rows, width d_model
@@ -240,6 +246,36 @@ twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, const float* u
                             const uint16_t* Wd, int32_t D, const float* dy, float l1_coeff,
                             float* dx, float* dWg_t, float* dWu_t, float* dWd, void* ws,
                             size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * Tensor-core variants of hybrid_ffn_fwd / hybrid_ffn_bwd (the paper's
+ * hybrid matmuls of section 2.B.3 mapped onto tcgen05 for activation
+ * densities at which every 128-token block touches every 128-neuron tile, so
+ * CUDA-core gathers of neuron rows cost more than dense tiles).  Same
+ * arguments, outputs and dense-row handling as the CUDA-core entry points;
+ * the ELL rows change:
+ *   dense-to-sparse products (u, and da in the backward) are full tensor-core
+ *   tiles X_ell W_u and dY_ell W_d^T of which only the ELL entries are kept;
+ *   sparse-to-dense products (y, dx, dW_g^T, dW_u^T, dW_d) expand the ELL
+ *   values tile by tile in shared memory into bf16 operands.
+ * The sparse values h u and du enter the tensor cores rounded to bf16
+ * (relative error up to 2^-8 each), as do dz and dy in the weight
+ * gradients; dy in da and dz in dx are split into bf16 hi and lo halves.
+ * Accumulation is fp32; results differ from the CUDA-core entry points by
+ * that rounding.  Requires
+ * D % 64 == 0 and C in {16, 32}; other shapes return TWELL_ERR_UNSUPPORTED.
+ * Deterministic for the ELL rows (no atomics); dense rows as above.
+ *   ws: twell_workspace_size(TWELL_WS_HYBRID_FWD_TC / _BWD_TC, ...) bytes.
+ */
+twell_status hybrid_ffn_fwd_tc(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,
+                               const uint16_t* Wd, int32_t D, float* y, float* u_ell,
+                               float* U_dense, void* ws, size_t ws_bytes, int32_t* status_dev,
+                               void* stream);
+twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h, const float* u_ell,
+                               const float* U_dense, const uint16_t* Wg_t, const uint16_t* Wu_t,
+                               const uint16_t* Wd, int32_t D, const float* dy, float l1_coeff,
+                               float* dx, float* dWg_t, float* dWu_t, float* dWd, void* ws,
+                               size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
  * hybrid_ffn_fwd with no workspace argument, for callers that cannot
