@@ -9,12 +9,13 @@
 //   warp 1      TMEM allocation and the MMA issue (one thread)
 //   warps 2-5   epilogue, one TMEM lane quarter each, two accumulators in
 //               flight
-//   warps 6-9   (expanded modes) write the bf16 A tile of each stage from the
-//               raw ELL slots: zero it and scatter the entries whose column
-//               falls in the K block, then fence to the async proxy and
-//               arrive.  They issue no global loads of their own, so the
-//               proxy fence has no loads in flight to wait for.
-//   warp 10     (expanded modes) TMA producer of the raw ELL slots (columns
+//   warps 6-13  (expanded modes) two groups of four warps, taking alternate
+//               stages, write the bf16 A tile of a stage from the raw ELL
+//               slots: zero it and scatter the entries whose column falls in
+//               the K block, then fence to the async proxy and arrive.  They
+//               issue no global loads of their own, so the proxy fence has no
+//               loads in flight to wait for.
+//   warp 14     (expanded modes) TMA producer of the raw ELL slots (columns
 //               and bf16 values of the rows of the stage) into a ring of
 //               their own, freed by the expansion warps: the raw data runs
 //               ahead of the A/B stages, which the MMA frees.
@@ -42,7 +43,7 @@ constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int kExpandBar = 1;     // named barrier of the expansion warps
+constexpr int kExpandBar = 1;     // named barriers 1, 2: the two expansion groups
 
 constexpr int RAW_COLS = 4096;  // raw slot: columns of <= 128 rows x C <= 32, then values
 
@@ -55,7 +56,7 @@ struct TcCfg {
   static constexpr int RAW_ROWS = MODE == TC_ROWS ? 128 : 64;
   static constexpr int RAW_SLOT = SAMPLE ? 0 : RAW_COLS + RAW_ROWS * 2 * 32;
   static constexpr int RAW_SLOTS = SAMPLE ? 0 : (MODE == TC_ROWS ? 2 : 4);
-  static constexpr int THREADS = SAMPLE ? 192 : 352;
+  static constexpr int THREADS = SAMPLE ? 192 : 480;
   static constexpr int SMEM =
       STAGES * STAGE_BYTES + STAGING + RAW_SLOTS * RAW_SLOT + 512 + 1024;
 };
@@ -131,7 +132,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
     }
     for (int r = 0; r < 4; ++r) {
       ptx::mbar_init(&raw_full[r], 1);
-      ptx::mbar_init(&raw_empty[r], 4);
+      // ROWS: both expansion groups read each slot (one half of the tile each)
+      ptx::mbar_init(&raw_empty[r], MODE == TC_ROWS ? 8 : 4);
     }
     ptx::fence_mbar_init();
   }
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
         ptx::mma_commit(&tfull[acc]);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == 14) {
     // ------------------------------------------- raw ELL slots (TMA) ring
     if (!Cfg::SAMPLE && lane == 0) {
       int slot = 0;
@@ -262,96 +264,102 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
     }
   } else if (warp >= 6) {
     // ------------------------------------------- ELL expansion into A tiles
+    // Two groups of four warps take alternate stages (group g the stages of
+    // odd or even sequence number), so each has two MMA stage times per tile.
     if (!Cfg::SAMPLE) {
-      const int x = threadIdx.x - 192;  // 0..127
+      const int grp = (warp - 6) >> 2;
+      const int x = (threadIdx.x - 192) & 127;  // thread within the group
       const uint32_t rr = static_cast<uint32_t>(x & 63);
-      int stage = 0, slot = 0;
+      const uint32_t bar_id = kExpandBar + static_cast<uint32_t>(grp);
+      int stage = 0, slot = 0, seq = 0;
       uint32_t phase = 0, rphase = 0;
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         int m_blk, n_blk, kb0, kb1;
         if (U.info(u, MODE, m_blk, n_blk, kb0, kb1) != 1) continue;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb, ++seq) {
           const int kl = kb % U.kb_per_seg;
-          const bool fresh = MODE == TC_TRANS || (kl & 1) == 0;  // first use of a raw slot
-          bool ok = ptx::mbar_wait(&empty[stage], phase ^ 1u);
-          if (fresh) ok = ok && ptx::mbar_wait(&raw_full[slot], rphase);
-          if (MODE == TC_TRANS ? ptx::bar_any(kExpandBar, 128, !ok)
-                               : !__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
-            goto done;
-          }
-          uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
-          const uint8_t* sr = raw + slot * Cfg::RAW_SLOT;
-          const uint16_t* rv = reinterpret_cast<const uint16_t*>(sr + RAW_COLS);
-          // Zero the A tile with contiguous 512-byte warp stores (conflict
-          // free): ROWS, each warp its own 32 rows (4 KB); TRANS, the whole
-          // tile across the four warps.
-          if (MODE == TC_ROWS) {
-            uint4* z = reinterpret_cast<uint4*>(sA + (x >> 5) * 4096) + lane;
+          // last use of the raw slot: ROWS, the second half of the tile (or
+          // the unit's last K block); TRANS, every K block
+          const bool slot_done = MODE == TC_TRANS || (kl & 1) == 1 || kb + 1 == kb1;
+          if ((seq & 1) == grp) {
+            const bool ok = ptx::mbar_wait(&empty[stage], phase ^ 1u) &&
+                            ptx::mbar_wait(&raw_full[slot], rphase);
+            if (MODE == TC_TRANS ? ptx::bar_any(bar_id, 128, !ok)
+                                 : !__all_sync(0xffffffffu, ok)) {
+              if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+              goto done;
+            }
+            uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
+            const uint8_t* sr = raw + slot * Cfg::RAW_SLOT;
+            const uint16_t* rv = reinterpret_cast<const uint16_t*>(sr + RAW_COLS);
+            // Zero the A tile with contiguous 512-byte warp stores (conflict
+            // free): ROWS, each warp its own 32 rows (4 KB); TRANS, the whole
+            // tile across the group.
+            if (MODE == TC_ROWS) {
+              uint4* z = reinterpret_cast<uint4*>(sA + (x >> 5) * 4096) + lane;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) z[32 * j] = make_uint4(0u, 0u, 0u, 0u);
-            __syncwarp();  // the warp's rows are zero before its lanes scatter into them
-          } else {
-            uint4* z = reinterpret_cast<uint4*>(sA) + x;
+              for (int j = 0; j < 8; ++j) z[32 * j] = make_uint4(0u, 0u, 0u, 0u);
+              __syncwarp();  // the warp's rows are zero before its lanes scatter into them
+            } else {
+              uint4* z = reinterpret_cast<uint4*>(sA) + x;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) z[128 * j] = make_uint4(0u, 0u, 0u, 0u);
-            ptx::bar_sync(kExpandBar, 128);  // the tile is zero before any scatter
-          }
-          // Slots of this thread: ROWS, row x of the tile (C / 16 groups of
-          // 16); TRANS, K row rr of the block, group x / 64.  Rows past the
-          // ELL rows read as all-0xff columns (no entries).  Each 4-slot word
-          // is skipped when no lane of the warp has an entry in it.
-          const int ngroups = MODE == TC_ROWS ? C / 16 : 1;
-          const int g0 = MODE == TC_ROWS ? 0 : (x >> 6) * 16;
-          const int srow = MODE == TC_ROWS ? x : static_cast<int>(rr);
-          const bool live = MODE == TC_ROWS
-                                ? m_blk * BM + x < U.n_rows
-                                : (kl * BK + static_cast<int>(rr) < U.n_rows && g0 < C);
-          const uint32_t half = static_cast<uint32_t>(kl & 1);
-          for (int gi = 0; gi < ngroups; ++gi) {
-            const int g = g0 + 16 * gi;
-            const uint4 cv = *reinterpret_cast<const uint4*>(sr + srow * C + g);
-            const uint4 v0 = *reinterpret_cast<const uint4*>(rv + srow * C + g);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(rv + srow * C + g + 8);
-            const uint32_t cw[4] = {live ? cv.x : ~0u, live ? cv.y : ~0u, live ? cv.z : ~0u,
-                                    live ? cv.w : ~0u};
-            const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+              for (int j = 0; j < 8; ++j) z[128 * j] = make_uint4(0u, 0u, 0u, 0u);
+              ptx::bar_sync(bar_id, 128);  // the tile is zero before any scatter
+            }
+            // Slots of this thread, loaded with 16-byte reads: ROWS, row x of
+            // the tile (C / 16 groups of 16 slots); TRANS, K row rr of the
+            // block, slot group x / 64.  Rows past the ELL rows read as
+            // 0xff columns.  Each 4-slot word is skipped when no lane of the
+            // warp has an entry of this A tile in it.
+            const int ngroups = MODE == TC_ROWS ? C / 16 : 1;
+            const int g0 = MODE == TC_ROWS ? 0 : (x >> 6) * 16;
+            const int srow = MODE == TC_ROWS ? x : static_cast<int>(rr);
+            const bool live = MODE == TC_ROWS
+                                  ? m_blk * BM + x < U.n_rows
+                                  : (kl * BK + static_cast<int>(rr) < U.n_rows && g0 < C);
+            const uint32_t half = static_cast<uint32_t>(kl & 1);
+            for (int gi = 0; gi < ngroups; ++gi) {
+              const int g = g0 + 16 * gi;
+              const uint4 cv = *reinterpret_cast<const uint4*>(sr + srow * C + g);
+              const uint4 v0 = *reinterpret_cast<const uint4*>(rv + srow * C + g);
+              const uint4 v1 = *reinterpret_cast<const uint4*>(rv + srow * C + g + 8);
+              const uint32_t cw[4] = {live ? cv.x : ~0u, live ? cv.y : ~0u, live ? cv.z : ~0u,
+                                      live ? cv.w : ~0u};
+              const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              // 0xff per byte whose column belongs to this A tile
-              const uint32_t hit =
-                  MODE == TC_ROWS ? __vcmpeq4(cw[q] & 0xc0c0c0c0u, half ? 0x40404040u : 0u)
-                                  : __vcmpltu4(cw[q], 0x80808080u);
-              if (!__any_sync(0xffffffffu, hit != 0u)) continue;
+              for (int q = 0; q < 4; ++q) {
+                // 0xff per slot byte that is an entry of this A tile
+                const uint32_t hit =
+                    MODE == TC_ROWS ? __vcmpeq4(cw[q] & 0xc0c0c0c0u, half ? 0x40404040u : 0u)
+                                    : __vcmpltu4(cw[q], 0x80808080u);
+                if (!__any_sync(0xffffffffu, hit != 0u)) continue;
 #pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                if (!((hit >> (8 * b)) & 1u)) continue;
-                const int e = 4 * q + b;
-                const uint32_t c = (cw[q] >> (8 * b)) & 0xffu;
-                const uint16_t v = static_cast<uint16_t>(vw[e >> 1] >> (16 * (e & 1)));
-                if (MODE == TC_ROWS) {
-                  // A row x, K = column c of tile half `half`
-                  const uint32_t k = c & 63u;
-                  *reinterpret_cast<uint16_t*>(
-                      sA + x * 128 + ((((k >> 3) ^ (x & 7)) << 4) | ((k & 7) << 1))) = v;
-                } else {
-                  // A row c (neuron of the tile), K = ELL row rr of the block
-                  *reinterpret_cast<uint16_t*>(
-                      sA + c * 128 + ((((rr >> 3) ^ (c & 7u)) << 4) | ((rr & 7) << 1))) = v;
+                for (int b = 0; b < 4; ++b) {
+                  if (!((hit >> (8 * b)) & 1u)) continue;
+                  const int e = 4 * q + b;
+                  const uint32_t c = (cw[q] >> (8 * b)) & 0xffu;
+                  const uint16_t v = static_cast<uint16_t>(vw[e >> 1] >> (16 * (e & 1)));
+                  if (MODE == TC_ROWS) {
+                    // A row x, K = column c of the stage's half
+                    const uint32_t k = c & 63u;
+                    *reinterpret_cast<uint16_t*>(
+                        sA + x * 128 + ((((k >> 3) ^ (x & 7)) << 4) | ((k & 7) << 1))) = v;
+                  } else {
+                    // A row c (neuron of the tile), K = ELL row rr of the block
+                    *reinterpret_cast<uint16_t*>(
+                        sA + c * 128 + ((((rr >> 3) ^ (c & 7u)) << 4) | ((rr & 7) << 1))) = v;
+                  }
                 }
               }
             }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(&ready[stage]);
+              if (MODE == TC_ROWS || slot_done) ptx::mbar_arrive(&raw_empty[slot]);
+            }
           }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(&ready[stage]);
-            // last use of the raw slot (ROWS: second half of the tile, or the
-            // unit's last K block)
-            if (MODE == TC_TRANS || (kl & 1) == 1 || kb + 1 == kb1)
-              ptx::mbar_arrive(&raw_empty[slot]);
-          }
-          if (MODE == TC_TRANS || (kl & 1) == 1 || kb + 1 == kb1) {
+          if (slot_done) {
             if (++slot == Cfg::RAW_SLOTS) {
               slot = 0;
               rphase ^= 1u;
@@ -391,6 +399,12 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
       if (Cfg::SAMPLE) {
+        // Row r of the tile is ELL row i.  Per (row, tile) the thread loads
+        // the C column indices, the h values (and for SAMPLE_DA the saved
+        // u) with 16-byte loads at once, then walks its slots for each
+        // 32-column accumulator chunk: slot s is an entry of chunk c iff
+        // s < count and its column's bits 5-6 equal c (columns ascending).
+        // Groups of four slots that no lane of the warp needs are skipped.
         const int i = m_blk * BM + r;
         const bool valid = i < U.n_rows;
 #pragma unroll 1
@@ -398,9 +412,39 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
           const int kt = n_blk * 2 + t2;
           if (kt >= p.n_t) break;  // uniform
           const size_t rt = static_cast<size_t>(valid ? i : 0) * p.n_t + kt;
-          const int cnt = valid ? p.ell_cnt[rt] : 0;
           const size_t base = rt * static_cast<size_t>(C);
-          int e = 0;
+          const int cnt = valid ? p.ell_cnt[rt] : 0;
+          uint32_t cw[8];
+          float hv[32], uv[32];
+          {
+            const uint4* cp = reinterpret_cast<const uint4*>(p.ell_col + base);
+            const float4* hp = reinterpret_cast<const float4*>(p.ell_val + base);
+            const float4* up = reinterpret_cast<const float4*>(p.u_ell + base);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const uint4 c4 = (g == 0 || C == 32) ? __ldg(cp + g) : make_uint4(~0u, ~0u, ~0u, ~0u);
+              cw[4 * g] = c4.x;
+              cw[4 * g + 1] = c4.y;
+              cw[4 * g + 2] = c4.z;
+              cw[4 * g + 3] = c4.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const bool in = q < 4 || C == 32;
+              const float4 h4 = in ? __ldg(hp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+              hv[4 * q] = h4.x;
+              hv[4 * q + 1] = h4.y;
+              hv[4 * q + 2] = h4.z;
+              hv[4 * q + 3] = h4.w;
+              if (MODE == TC_SAMPLE_DA) {
+                const float4 u4 = in ? __ldg(up + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                uv[4 * q] = u4.x;
+                uv[4 * q + 1] = u4.y;
+                uv[4 * q + 2] = u4.z;
+                uv[4 * q + 3] = u4.w;
+              }
+            }
+          }
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
@@ -410,29 +454,35 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
             for (int j = 0; j < 8; ++j)
               *reinterpret_cast<uint4*>(my_stage + ((j ^ (r & 7)) << 4)) =
                   make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            const int hi = 32 * (c + 1);
-            while (e < cnt) {
-              const int col = p.ell_col[base + e];
-              if (col >= hi) break;
-              const int cl = col & 31;
-              const float val = *reinterpret_cast<const float*>(
-                  my_stage + ((((cl >> 2) ^ (r & 7)) << 4) | ((cl & 3) << 2)));
-              const size_t pos = base + e;
-              const float hv = p.ell_val[pos];
-              if (MODE == TC_SAMPLE_U) {
-                p.u_ell[pos] = val;
-                p.a_ell[pos] = bf16_bits(hv * val);
-              } else {
-                const float uv = p.u_ell[pos];
-                const float dz = fmaf(val, uv, p.lambda);
-                const uint16_t dz_hi = bf16_bits(dz);
-                p.dz_ell[pos] = dz_hi;
-                p.dz_lo_ell[pos] = bf16_bits(dz - __uint_as_float(static_cast<uint32_t>(dz_hi)
-                                                                   << 16));
-                p.du_ell[pos] = bf16_bits(val * hv);
-                p.a_ell[pos] = bf16_bits(hv * uv);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              // 0xff per slot byte of word q that is an entry of chunk c
+              const uint32_t w = cw[q];
+              const uint32_t in_chunk = __vcmpeq4(w & 0xe0e0e0e0u, static_cast<uint32_t>(c) *
+                                                                   0x20202020u);
+              const uint32_t live = (4 * q < cnt) ? in_chunk : 0u;
+              if (!__any_sync(0xffffffffu, live != 0u)) continue;
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const int sidx = 4 * q + b;
+                if (sidx >= cnt || !((live >> (8 * b)) & 1u)) continue;
+                const int cl = (w >> (8 * b)) & 31;
+                const float val = *reinterpret_cast<const float*>(
+                    my_stage + ((((cl >> 2) ^ (r & 7)) << 4) | ((cl & 3) << 2)));
+                const size_t pos = base + sidx;
+                if (MODE == TC_SAMPLE_U) {
+                  p.u_ell[pos] = val;
+                  p.a_ell[pos] = bf16_bits(hv[sidx] * val);
+                } else {
+                  const float dz = fmaf(val, uv[sidx], p.lambda);
+                  const uint16_t dz_hi = bf16_bits(dz);
+                  p.dz_ell[pos] = dz_hi;
+                  p.dz_lo_ell[pos] =
+                      bf16_bits(dz - __uint_as_float(static_cast<uint32_t>(dz_hi) << 16));
+                  p.du_ell[pos] = bf16_bits(val * hv[sidx]);
+                  p.a_ell[pos] = bf16_bits(hv[sidx] * uv[sidx]);
+                }
               }
-              ++e;
             }
           }
         }
