@@ -106,7 +106,14 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
     p.ell_cnt[dst_rt + k] = static_cast<uint8_t>(c);
     float* dv = p.ell_val + (dst_rt + k) * p.C;
     uint8_t* dc = p.ell_col + (dst_rt + k) * p.C;
-    for (int s = c; s < p.C; ++s) dc[s] = 0xffu;  // padding slots: column sentinel
+    // padding slots: column sentinel 0xff (whole rows of 16 bytes first,
+    // entries overwrite theirs below)
+    if ((p.C & 15) == 0) {
+      for (int s = (c & ~15); s < p.C; s += 16)
+        *reinterpret_cast<uint4*>(dc + s) = make_uint4(~0u, ~0u, ~0u, ~0u);
+    } else {
+      for (int s = c; s < p.C; ++s) dc[s] = 0xffu;
+    }
     if (c <= p.W) {
       const float* sv = p.val + (src_rt + k) * p.W;
       const uint8_t* sc = p.col + (src_rt + k) * p.W;
@@ -174,7 +181,8 @@ twell_status check_hybrid(const hybrid_t* h, int32_t T, int32_t F) {
     return TWELL_ERR_INVALID;
   if (h->max_dense > 0 && (!h->dense_rows || !h->dense_h || !aligned16(h->dense_h)))
     return TWELL_ERR_INVALID;
-  if (!aligned16(h->ell_val) || !aligned16(h->row_map) || !aligned16(h->ell_rows))
+  if (!aligned16(h->ell_val) || !aligned16(h->row_map) || !aligned16(h->ell_rows) ||
+      !aligned16(h->ell_col) || !aligned16(h->ell_cnt))
     return TWELL_ERR_INVALID;
   return TWELL_OK;
 }

@@ -279,7 +279,9 @@ def run_train(args, dev, flush, stream):
     """Training step of the 2B-class layer (T=16384, D=2304, F=9216, mean 5%
     active, 3% of rows above the ELL capacity C=32): gate GEMM with TwELL
     epilogue (W=32), TwELL->hybrid, hybrid forward, hybrid backward with the
-    L1 term.  Returns a dict for the JSON line (per-kernel event times)."""
+    L1 term.  Both variants of the hybrid matmuls are timed: the tensor-core
+    one (hybrid_ffn_*_tc, the headline) and the CUDA-core one.  Returns a
+    dict for the JSON line (per-kernel event times, peak memory)."""
     import torch
 
     import activation_sparse_gated_gate_gb300 as tw
@@ -293,86 +295,97 @@ def run_train(args, dev, flush, stream):
 
     x, Wg, Wu, Wd = up(w.x), up(w.Wg_t), up(w.Wu_t), up(w.Wd)
     dy = torch.from_numpy(w.dy).to(dev)
-    torch.cuda.synchronize()
-    mem_base = torch.cuda.memory_allocated()
-    torch.cuda.reset_peak_memory_stats()
     max_dense = 1024
-    h = tw.TwELL(w.T, w.F, w.cap, device=dev)
-    hyb = tw.Hybrid(w.T, w.F, w.cap, max_dense, device=dev)
     f32 = torch.float32
-    y = torch.empty((w.T, w.D), dtype=f32, device=dev)
-    u_ell = torch.empty((w.T, w.F // 128, w.cap), dtype=f32, device=dev)
-    U_dense = torch.empty((max_dense, w.F), dtype=f32, device=dev)
-    dx = torch.empty((w.T, w.D), dtype=f32, device=dev)
-    dW = [torch.empty((w.F, w.D), dtype=f32, device=dev) for _ in range(3)]
-    ws_f = tw._workspace(tw.twell_workspace_size(tw.WS_HYBRID_FWD, w.T, w.D, w.F, w.cap,
-                                                 max_dense), dev)
-    ws_b = tw._workspace(tw.twell_workspace_size(tw.WS_HYBRID_BWD, w.T, w.D, w.F, w.cap,
-                                                 max_dense), dev)
-    names = ["twell_gate_pack", "twell_to_hybrid", "hybrid_ffn_fwd", "hybrid_ffn_bwd"]
-
-    def launch(i):
-        if i == 0:
-            tw.twell_gate_pack(x, Wg, h, stream=stream)
-        elif i == 1:
-            tw.twell_to_hybrid(h, hyb, stream=stream)
-        elif i == 2:
-            tw.hybrid_ffn_fwd(x, hyb, Wu, Wd, y=y, u_ell=u_ell, U_dense=U_dense, ws=ws_f,
-                              stream=stream)
-        else:
-            tw.hybrid_ffn_bwd(x, hyb, u_ell, U_dense, Wg, Wu, Wd, dy, w.l1_coeff, dx=dx,
-                              dWg_t=dW[0], dWu_t=dW[1], dWd=dW[2], ws=ws_b, stream=stream)
-
-    flush.zero_()
-    for i in range(4):
-        launch(i)
-    torch.cuda.synchronize()
-    # every buffer of the step is the caller's (the library allocates none);
-    # the flush buffer predates the baseline
-    mem_ours = torch.cuda.max_memory_allocated() - mem_base
-    for _ in range(max(1, args.warmup)):
-        flush.zero_()
-        for i in range(4):
-            launch(i)
-    torch.cuda.synchronize()
-    if int(h.status.item()) or int(hyb.status.item()):
-        raise RuntimeError("device status flags set in the training step")
     K = args.train_steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    for k in range(K):
+    ws_n = int(os.environ.get("WORLD_SIZE", "1"))
+    variants = {
+        "tensor-core": (tw.hybrid_ffn_fwd_tc, tw.hybrid_ffn_bwd_tc, tw.WS_HYBRID_FWD_TC,
+                        tw.WS_HYBRID_BWD_TC),
+        "cuda-core": (tw.hybrid_ffn_fwd, tw.hybrid_ffn_bwd, tw.WS_HYBRID_FWD,
+                      tw.WS_HYBRID_BWD),
+    }
+    names = ["twell_gate_pack", "twell_to_hybrid", "hybrid_ffn_fwd", "hybrid_ffn_bwd"]
+    out = {}
+    for vname, (fwd, bwd, op_f, op_b) in variants.items():
+        torch.cuda.synchronize()
+        mem_base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        h = tw.TwELL(w.T, w.F, w.cap, device=dev)
+        hyb = tw.Hybrid(w.T, w.F, w.cap, max_dense, device=dev)
+        y = torch.empty((w.T, w.D), dtype=f32, device=dev)
+        u_ell = torch.empty((w.T, w.F // 128, w.cap), dtype=f32, device=dev)
+        U_dense = torch.empty((max_dense, w.F), dtype=f32, device=dev)
+        dx = torch.empty((w.T, w.D), dtype=f32, device=dev)
+        dW = [torch.empty((w.F, w.D), dtype=f32, device=dev) for _ in range(3)]
+        ws_f = tw._workspace(tw.twell_workspace_size(op_f, w.T, w.D, w.F, w.cap, max_dense), dev)
+        ws_b = tw._workspace(tw.twell_workspace_size(op_b, w.T, w.D, w.F, w.cap, max_dense), dev)
+
+        def launch(i):
+            if i == 0:
+                tw.twell_gate_pack(x, Wg, h, stream=stream)
+            elif i == 1:
+                tw.twell_to_hybrid(h, hyb, stream=stream)
+            elif i == 2:
+                fwd(x, hyb, Wu, Wd, y=y, u_ell=u_ell, U_dense=U_dense, ws=ws_f, stream=stream)
+            else:
+                bwd(x, hyb, u_ell, U_dense, Wg, Wu, Wd, dy, w.l1_coeff, dx=dx, dWg_t=dW[0],
+                    dWu_t=dW[1], dWd=dW[2], ws=ws_b, stream=stream)
+
         flush.zero_()
-        ev[k][0].record(stream)
         for i in range(4):
             launch(i)
-            ev[k][i + 1].record(stream)
-    torch.cuda.synchronize()
-    per = {n: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
-           for i, n in enumerate(names)}
-    ms = max_over_ranks(sum(per.values()), dev)
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    nnz = int(h.cnt.to(torch.int64).sum().item())
-    n_dense = hyb.n_dense
-    del h, hyb, y, u_ell, U_dense, dx, dW, ws_f, ws_b
-    torch.cuda.empty_cache()
+        torch.cuda.synchronize()
+        # every buffer of the step is the caller's (the library allocates none);
+        # the flush buffer predates the baseline
+        mem = torch.cuda.max_memory_allocated() - mem_base
+        for _ in range(max(1, args.warmup)):
+            flush.zero_()
+            for i in range(4):
+                launch(i)
+        torch.cuda.synchronize()
+        if int(h.status.item()) or int(hyb.status.item()):
+            raise RuntimeError(f"device status flags set in the {vname} training step")
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            for i in range(4):
+                launch(i)
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = {n: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+               for i, n in enumerate(names)}
+        ms = max_over_ranks(sum(per.values()), dev)
+        out[vname] = {"ms_per_step": ms, "tokens_per_s": job_tokens_per_s(w.T, ws_n, ms),
+                      "kernels_ms": per, "peak_memory_bytes": mem}
+        nnz = int(h.cnt.to(torch.int64).sum().item())
+        n_dense = hyb.n_dense
+        del h, hyb, y, u_ell, U_dense, dx, dW, ws_f, ws_b
+        torch.cuda.empty_cache()
     d_ms, d_mem = dense_context_train(x, Wg, Wu, Wd, dy, w.l1_coeff, flush, stream, 2, K)
+    head = out["tensor-core"]
     return {
         "metric": "sparse gated-FFN training step (fwd+bwd) tokens/s per layer",
-        "value": job_tokens_per_s(w.T, ws, ms), "unit": "tokens/s", "ms_per_step": ms,
+        "value": head["tokens_per_s"], "unit": "tokens/s", "ms_per_step": head["ms_per_step"],
         "steps": K, "scaling": "weak",
         "dtype": "bf16 in, fp32 accumulate / gradients",
+        "variant": "tensor-core hybrid matmuls (hybrid_ffn_fwd_tc / hybrid_ffn_bwd_tc)",
         "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F, "cap": w.cap,
                    "l1_coeff": w.l1_coeff, "nnz": nnz, "density": nnz / (w.T * w.F),
                    "n_dense": n_dense, "max_dense": max_dense,
                    "l2": "flushed (512 MiB write) before every step"},
-        "kernels_ms": per,
+        "kernels_ms": head["kernels_ms"],
+        "cuda_core": out["cuda-core"],
         "peak_memory": {
-            "ours_bytes": mem_ours, "dense_torch_bytes": d_mem,
-            "ratio": mem_ours / d_mem if d_mem else None,
+            "tensor_core_bytes": head["peak_memory_bytes"],
+            "cuda_core_bytes": out["cuda-core"]["peak_memory_bytes"],
+            "dense_torch_bytes": d_mem,
             "scope": ("device bytes the step allocates above its inputs (x, dy) and bf16 "
                       "weights: ours = TwELL + hybrid + y + u + dense-row U + dx + fp32 dW + "
                       "workspaces; dense = torch autograd activations + bf16 grads")},
         "dense_context": {
-            "ms_per_step": d_ms, "tokens_per_s": job_tokens_per_s(w.T, ws, d_ms),
+            "ms_per_step": d_ms, "tokens_per_s": job_tokens_per_s(w.T, ws_n, d_ms),
             "what": "torch bf16 autograd fwd+bwd of the dense gated FFN (cuBLAS), context only"},
     }
 
