@@ -68,13 +68,23 @@ twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
                                uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                                uint64_t pitch) {
   return make_tmap_2d(map, 2, base, inner, outer, box_inner, box_outer,
-                      (pitch ? pitch : inner) * 2, true);
+                      (pitch ? pitch : inner) * 2, 128);
 }
 
 twell_status make_tmap_2d(CUtensorMap* map, int elem_bytes, const void* base, uint64_t inner,
                           uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                          uint64_t pitch_bytes, bool swizzle128) {
+                          uint64_t pitch_bytes, int swizzle) {
   if (elem_bytes != 1 && elem_bytes != 2) return TWELL_ERR_INVALID;
+  CUtensorMapSwizzle sw;
+  switch (swizzle) {
+    case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    default: return TWELL_ERR_INVALID;
+  }
+  if (swizzle && box_inner * static_cast<uint32_t>(elem_bytes) > static_cast<uint32_t>(swizzle))
+    return TWELL_ERR_INVALID;
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -90,8 +100,7 @@ twell_status make_tmap_2d(CUtensorMap* map, int elem_bytes, const void* base, ui
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(
       map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TWELL_OK : TWELL_ERR_INVALID;
 }

@@ -43,9 +43,12 @@ twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
 
 // 2-D tensor map of 1-byte (u8) or 2-byte (bf16) elements over a row-major
 // [outer][inner] array with rows `pitch_bytes` apart (a multiple of 16), box
-// [box_outer][box_inner], 128-byte swizzle or none, zero fill out of bounds.
+// [box_outer][box_inner], zero fill out of bounds.  `swizzle` = 0 (none) or
+// the span in bytes (32, 64, 128): in shared memory, the 16-byte chunk index
+// within each span is XORed with address bits 7 and up (as many bits as the
+// span has chunk-index bits); the inner box must fit in the span.
 twell_status make_tmap_2d(CUtensorMap* map, int elem_bytes, const void* base, uint64_t inner,
                           uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                          uint64_t pitch_bytes, bool swizzle128);
+                          uint64_t pitch_bytes, int swizzle);
 
 }  // namespace twell

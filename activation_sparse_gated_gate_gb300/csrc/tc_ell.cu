@@ -9,13 +9,13 @@
 //   warp 1      TMEM allocation and the MMA issue (one thread)
 //   warps 2-5   epilogue, one TMEM lane quarter each, two accumulators in
 //               flight
-//   warps 6-13  (expanded modes) two groups of four warps, taking alternate
-//               stages, write the bf16 A tile of a stage from the raw ELL
+//   warps 6-21  (expanded modes) four groups of four warps, taking the stages
+//               in turn, write the bf16 A tile of a stage from the raw ELL
 //               slots: zero it and scatter the entries whose column falls in
 //               the K block, then fence to the async proxy and arrive.  They
 //               issue no global loads of their own, so the proxy fence has no
 //               loads in flight to wait for.
-//   warp 14     (expanded modes) TMA producer of the raw ELL slots (columns
+//   warp 22     (expanded modes) TMA producer of the raw ELL slots (columns
 //               and bf16 values of the rows of the stage) into a ring of
 //               their own, freed by the expansion warps: the raw data runs
 //               ahead of the A/B stages, which the MMA frees.
@@ -43,7 +43,9 @@ constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int kExpandBar = 1;     // named barriers 1, 2: the two expansion groups
+constexpr int kExpandBar = 1;     // named barriers 1 .. kGroups: the expansion groups
+constexpr int kGroups = 4;        // expansion groups of four warps, taking stages in turn
+constexpr int kRawWarp = 6 + 4 * kGroups;
 
 constexpr int RAW_COLS = 4096;  // raw slot: columns of <= 128 rows x C <= 32, then values
 
@@ -56,7 +58,7 @@ struct TcCfg {
   static constexpr int RAW_ROWS = MODE == TC_ROWS ? 128 : 64;
   static constexpr int RAW_SLOT = SAMPLE ? 0 : RAW_COLS + RAW_ROWS * 2 * 32;
   static constexpr int RAW_SLOTS = SAMPLE ? 0 : (MODE == TC_ROWS ? 2 : 4);
-  static constexpr int THREADS = SAMPLE ? 192 : 480;
+  static constexpr int THREADS = SAMPLE ? 192 : 32 * (kRawWarp + 1);
   static constexpr int SMEM =
       STAGES * STAGE_BYTES + STAGING + RAW_SLOTS * RAW_SLOT + 512 + 1024;
 };
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
     for (int r = 0; r < 4; ++r) {
       ptx::mbar_init(&raw_full[r], 1);
       // ROWS: both expansion groups read each slot (one half of the tile each)
-      ptx::mbar_init(&raw_empty[r], MODE == TC_ROWS ? 8 : 4);
+      ptx::mbar_init(&raw_empty[r], MODE == TC_ROWS ? 8 : 4);  // ROWS: the two groups of a tile
     }
     ptx::fence_mbar_init();
   }
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
         ptx::mma_commit(&tfull[acc]);
       }
     }
-  } else if (warp == 14) {
+  } else if (warp == kRawWarp) {
     // ------------------------------------------- raw ELL slots (TMA) ring
     if (!Cfg::SAMPLE && lane == 0) {
       int slot = 0;
@@ -264,8 +266,9 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
     }
   } else if (warp >= 6) {
     // ------------------------------------------- ELL expansion into A tiles
-    // Two groups of four warps take alternate stages (group g the stages of
-    // odd or even sequence number), so each has two MMA stage times per tile.
+    // kGroups groups of four warps take the stages in turn (group g the
+    // stages with sequence number = g mod kGroups), so each has kGroups MMA
+    // stage times per tile.
     if (!Cfg::SAMPLE) {
       const int grp = (warp - 6) >> 2;
       const int x = (threadIdx.x - 192) & 127;  // thread within the group
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
           // last use of the raw slot: ROWS, the second half of the tile (or
           // the unit's last K block); TRANS, every K block
           const bool slot_done = MODE == TC_TRANS || (kl & 1) == 1 || kb + 1 == kb1;
-          if ((seq & 1) == grp) {
+          if (seq % kGroups == grp) {
             const bool ok = ptx::mbar_wait(&empty[stage], phase ^ 1u) &&
                             ptx::mbar_wait(&raw_full[slot], rphase);
             if (MODE == TC_TRANS ? ptx::bar_any(bar_id, 128, !ok)
@@ -318,11 +321,18 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
                                   ? m_blk * BM + x < U.n_rows
                                   : (kl * BK + static_cast<int>(rr) < U.n_rows && g0 < C);
             const uint32_t half = static_cast<uint32_t>(kl & 1);
+            // chunk j of a raw row lies at chunk j ^ (the row's address bits
+            // 7..): columns (32-byte rows, C == 32) (row >> 2) & 1; values
+            // (2C-byte rows) (row >> 1) & 3 for C == 32, (row >> 2) & 1 for 16
+            const int cswz = C == 32 ? (srow >> 2) & 1 : 0;
+            const int vswz = C == 32 ? (srow >> 1) & 3 : (srow >> 2) & 1;
             for (int gi = 0; gi < ngroups; ++gi) {
-              const int g = g0 + 16 * gi;
-              const uint4 cv = *reinterpret_cast<const uint4*>(sr + srow * C + g);
-              const uint4 v0 = *reinterpret_cast<const uint4*>(rv + srow * C + g);
-              const uint4 v1 = *reinterpret_cast<const uint4*>(rv + srow * C + g + 8);
+              const int cj = (g0 >> 4) + gi;  // 16-slot group = column chunk
+              const uint4 cv =
+                  *reinterpret_cast<const uint4*>(sr + srow * C + 16 * (cj ^ cswz));
+              const uint8_t* vr = reinterpret_cast<const uint8_t*>(rv) + 2 * srow * C;
+              const uint4 v0 = *reinterpret_cast<const uint4*>(vr + 16 * ((2 * cj) ^ vswz));
+              const uint4 v1 = *reinterpret_cast<const uint4*>(vr + 16 * ((2 * cj + 1) ^ vswz));
               const uint32_t cw[4] = {live ? cv.x : ~0u, live ? cv.y : ~0u, live ? cv.z : ~0u,
                                       live ? cv.w : ~0u};
               const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -553,28 +563,31 @@ bool tc_supported(int32_t D, int32_t F, int32_t C) {
 
 twell_status tc_map_a(CUtensorMap* m, const uint16_t* base, int64_t rows, int64_t D,
                       int64_t pitch) {
-  return make_tmap_2d(m, 2, base, D, rows, BK, BM, (pitch ? pitch : D) * 2, true);
+  return make_tmap_2d(m, 2, base, D, rows, BK, BM, (pitch ? pitch : D) * 2, 128);
 }
 
 twell_status tc_map_w_kmajor(CUtensorMap* m, const uint16_t* base, int64_t F, int64_t D) {
-  return make_tmap_2d(m, 2, base, D, F, BK, BN, D * 2, true);
+  return make_tmap_2d(m, 2, base, D, F, BK, BN, D * 2, 128);
 }
 
 twell_status tc_map_mn(CUtensorMap* m, const uint16_t* base, int64_t rows, int64_t D,
                        int64_t pitch) {
-  return make_tmap_2d(m, 2, base, D, rows, 64, BK, (pitch ? pitch : D) * 2, true);
+  return make_tmap_2d(m, 2, base, D, rows, 64, BK, (pitch ? pitch : D) * 2, 128);
 }
 
+// Raw ELL boxes land swizzled so that a thread reading its own row's 16-byte
+// chunks hits distinct bank groups: columns (C bytes per row) with the 32-byte
+// swizzle when C == 32, values (2 C bytes per row) with the 2 C-byte swizzle.
 twell_status tc_map_cols(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t n_t,
                          int64_t C, int box_rows) {
   return make_tmap_2d(m, 1, base, n_t * C, rows, static_cast<uint32_t>(C),
-                      static_cast<uint32_t>(box_rows), n_t * C, false);
+                      static_cast<uint32_t>(box_rows), n_t * C, C == 32 ? 32 : 0);
 }
 
 twell_status tc_map_vals(CUtensorMap* m, const uint16_t* base, int64_t rows, int64_t n_t,
                          int64_t C, int box_rows) {
   return make_tmap_2d(m, 2, base, n_t * C, rows, static_cast<uint32_t>(C),
-                      static_cast<uint32_t>(box_rows), n_t * C * 2, false);
+                      static_cast<uint32_t>(box_rows), n_t * C * 2, static_cast<int>(2 * C));
 }
 
 twell_status tc_run(const TcMaps& maps, const TcArgs& a, const DeviceInfo& dev,
