@@ -9,7 +9,7 @@ namespace twell {
 struct WsLayout {
   size_t bytes = 0;
   // tensor-core ELL path: gathered bf16 x / dy rows, bf16 ELL values
-  size_t xe = 0, dye = 0, ae = 0, dze = 0, dzl = 0, due = 0;
+  size_t xe = 0, dye = 0, ae = 0, ale = 0, dze = 0, dzl = 0, due = 0;
   // forward
   size_t xo = 0, wdT = 0, asplit = 0;
   // backward
@@ -45,6 +45,7 @@ inline WsLayout ws_layout(int op, int64_t T, int64_t D, int64_t F, int64_t cap,
   }
   if (op == 4) {
     w.dye = ws_take(&cur, T * 2 * D * 2);  // bf16 [hi | lo] rows
+    w.ale = ws_take(&cur, T * n_t * cap * 2);
     w.dze = ws_take(&cur, T * n_t * cap * 2);
     w.dzl = ws_take(&cur, T * n_t * cap * 2);
     w.due = ws_take(&cur, T * n_t * cap * 2);

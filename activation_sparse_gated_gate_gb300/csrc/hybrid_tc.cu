@@ -16,14 +16,16 @@
 //              lambda (bf16 hi and lo), du = da h, a = h u (bf16)
 //   ROWS       dx[ell rows] = E(dz_hi) W_g^T + E(dz_lo) W_g^T + E(du) W_u^T
 //   TRANS x3   dW_g^T = E(dz_hi)^T Xe + E(dz_lo)^T Xe, dW_u^T = E(du)^T Xe,
-//              dW_d = E(a)^T dYe_hi + E(a)^T dYe_lo
+//              dW_d = E(a_hi)^T dYe_hi + E(a_lo)^T dYe_hi + E(a_hi)^T dYe_lo
 // dy and dz keep their low halves: a column of W_g with large entries for
 // every neuron (a bias feature) sums dz into dx, where a single bf16
 // rounding of each term would dominate the column's error, and dz = da u is
 // the most heavy-tailed of the sparse values (a product of two roughly
 // normal factors), so in dW_g a few large terms can carry the rounding of
-// an element.  In dW_d both factors are rounded activations; keeping dy's
-// low half leaves one bf16 rounding per term.
+// an element.  In dW_d both factors are activations; their low halves (the
+// a_lo dy_lo product is below fp32 resolution and left out) keep the
+// heavy-tailed terms that dominate some elements from carrying a bf16
+// rounding each.
 // E(v) = the ELL values expanded to dense bf16 tiles in shared memory.
 // Dense overflow rows: the shared tensor-core path with hi/lo splits, which
 // writes its dx rows and adds its weight-gradient terms after TRANS.
@@ -169,6 +171,7 @@ extern "C" twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h,
   uint16_t* Xe = reinterpret_cast<uint16_t*>(w + L.xe);
   uint16_t* dYe = reinterpret_cast<uint16_t*>(w + L.dye);
   uint16_t* Ae = reinterpret_cast<uint16_t*>(w + L.ae);
+  uint16_t* Al = reinterpret_cast<uint16_t*>(w + L.ale);
   uint16_t* dZe = reinterpret_cast<uint16_t*>(w + L.dze);
   uint16_t* dZl = reinterpret_cast<uint16_t*>(w + L.dzl);
   uint16_t* dUe = reinterpret_cast<uint16_t*>(w + L.due);
@@ -185,6 +188,7 @@ extern "C" twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h,
     a.nseg = 2;
     a.u_ell = const_cast<float*>(u_ell);
     a.a_ell = Ae;
+    a.a_lo_ell = Al;
     a.dz_ell = dZe;
     a.dz_lo_ell = dZl;
     a.du_ell = dUe;
@@ -210,14 +214,14 @@ extern "C" twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h,
   {  // weight gradients of the ELL rows (overwrite)
     struct Job {
       int nseg;
-      const uint16_t* vals[2];
-      const uint16_t* b[2];
+      const uint16_t* vals[3];
+      const uint16_t* b[3];
       int64_t pitch;
       float* out;
     };
-    const Job jobs[3] = {{2, {dZe, dZl}, {Xe, Xe}, D, dWg_t},
-                         {1, {dUe, nullptr}, {Xe, nullptr}, D, dWu_t},
-                         {2, {Ae, Ae}, {dYe, dYe + D}, D2, dWd}};
+    const Job jobs[3] = {{2, {dZe, dZl, nullptr}, {Xe, Xe, nullptr}, D, dWg_t},
+                         {1, {dUe, nullptr, nullptr}, {Xe, nullptr, nullptr}, D, dWu_t},
+                         {3, {Ae, Al, Ae}, {dYe, dYe, dYe + D}, D2, dWd}};
     for (const Job& jb : jobs) {
       TcMaps m;
       TcArgs a = tc_args(TC_TRANS, h, D, status_dev);

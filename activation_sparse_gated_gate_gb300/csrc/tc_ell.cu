@@ -490,7 +490,11 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
                   p.dz_lo_ell[pos] =
                       bf16_bits(dz - __uint_as_float(static_cast<uint32_t>(dz_hi) << 16));
                   p.du_ell[pos] = bf16_bits(val * hv[sidx]);
-                  p.a_ell[pos] = bf16_bits(hv[sidx] * uv[sidx]);
+                  const float a = hv[sidx] * uv[sidx];
+                  const uint16_t a_hi = bf16_bits(a);
+                  p.a_ell[pos] = a_hi;
+                  p.a_lo_ell[pos] =
+                      bf16_bits(a - __uint_as_float(static_cast<uint32_t>(a_hi) << 16));
                 }
               }
             }

@@ -22,7 +22,7 @@ enum TcMode : int32_t {
   // acc = sum_s dY_s W_d^T (M = ELL rows, N = F, K = D per segment; the
   // segments are the bf16 hi and lo halves of dy); at the entries:
   // du = acc h, dz = acc u + lambda, a = h u -> dz_ell (hi) + dz_lo_ell (lo),
-  // du_ell, a_ell (bf16)
+  // du_ell, a_ell (hi) + a_lo_ell (lo) (bf16)
   TC_SAMPLE_DA = 1,
   // out[row_idx[i]][:] = sum_s E_s[i][:] W_s (M = ELL rows, N = D, K = F per
   // segment, up to 3 segments), E_s = ELL values vals_s expanded to dense
@@ -56,6 +56,7 @@ struct TcArgs {
   const float* ell_val;
   float* u_ell;            // SAMPLE_U out, SAMPLE_DA in
   uint16_t* a_ell;         // bf16 h u, out of both
+  uint16_t* a_lo_ell;      // SAMPLE_DA out: bf16(h u - bf16(h u))
   uint16_t* dz_ell;        // SAMPLE_DA out: bf16(dz)
   uint16_t* dz_lo_ell;     // SAMPLE_DA out: bf16(dz - bf16(dz))
   uint16_t* du_ell;        // SAMPLE_DA out

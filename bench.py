@@ -41,7 +41,7 @@ METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of ro
 # is the one captured (sha256 of the .cu file); otherwise reported as null.
 TRAFFIC = {
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        108.99e6, "csrc/ffn_fwd.cu", "605af6fc80c09d5d", "profiles/ffn_fwd_0.5B_T8192.md"),
+        108.68e6, "csrc/ffn_fwd.cu", "67352d39d43dce0a", "profiles/ffn_fwd_0.5B_T8192.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         45.50e6, "csrc/gate_pack.cu", "eb007b4c884b853e", "profiles/gate_pack_0.5B_T8192.md"),
 }
@@ -78,8 +78,9 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=200):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
 
@@ -87,7 +88,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -127,6 +128,47 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+    def watts(self):
+        """Mean board power (nvidia-smi power.draw) over the samples, or None."""
+        w = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) >= 4:
+                try:
+                    w.append(float(f[3]))
+                except ValueError:
+                    pass
+        return statistics.mean(w) if w else None
+
+
+def energy_per_token(fn, tokens, stream, dev_index, seconds=1.5):
+    """Board energy per token of back-to-back steps fn(): mean nvidia-smi
+    power.draw (sampled every 100 ms) times the steps' CUDA-event time,
+    divided by the tokens processed.  Idle board power is included."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    n = max(1, int(seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
+    with ClockSampler(dev_index, interval_ms=100) as clk:
+        time.sleep(0.3)  # let the sampler start before the loop
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    w = clk.watts()
+    if w is None:
+        return None
+    return {"joules_per_token": w * ms * 1e-3 / (n * tokens), "watts": w,
+            "steps": n, "ms_per_step": ms / n}
 
 
 def max_over_ranks(value, device=None):
@@ -311,7 +353,9 @@ def run_train(args, dev, flush, stream):
         torch.cuda.synchronize()
         mem_base = torch.cuda.memory_allocated()
         torch.cuda.reset_peak_memory_stats()
-        h = tw.TwELL(w.T, w.F, w.cap, device=dev)
+        # TwELL width = ELL capacity: only dense-backup rows spill, at most
+        # max_dense * n_t slices
+        h = tw.TwELL(w.T, w.F, w.cap, spill_cap=max_dense * (w.F // 128), device=dev)
         hyb = tw.Hybrid(w.T, w.F, w.cap, max_dense, device=dev)
         y = torch.empty((w.T, w.D), dtype=f32, device=dev)
         u_ell = torch.empty((w.T, w.F // 128, w.cap), dtype=f32, device=dev)
@@ -387,6 +431,77 @@ def run_train(args, dev, flush, stream):
         "dense_context": {
             "ms_per_step": d_ms, "tokens_per_s": job_tokens_per_s(w.T, ws_n, d_ms),
             "what": "torch bf16 autograd fwd+bwd of the dense gated FFN (cuBLAS), context only"},
+    }
+
+
+def run_stack(args, dev, flush, stream, layers=4):
+    """A residual stack of `layers` 2B-class FFN layers (T=16384, D=2304,
+    F=9216, 5 % mean density, 3 % dense rows, C=32), trained through the
+    torch.autograd wrapper (tensor-core hybrid) against the same stack as
+    dense torch bf16 autograd (cuBLAS).  One step = forward + backward of
+    all layers with the L1 term.  Returns a dict for the JSON line."""
+    import torch
+
+    from activation_sparse_gated_gate_gb300.autograd import SparseFFNStack
+    import workloads
+
+    ws = []
+    for l in range(layers):
+        wl = workloads.config(3, seed=l)
+        if l == 0:
+            w0 = wl
+        ws.append(tuple(torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.bfloat16).to(dev) for a in (wl.Wg_t, wl.Wu_t, wl.Wd)))
+    x = torch.from_numpy(np.ascontiguousarray(w0.x).view(np.int16)).view(torch.bfloat16).to(dev)
+    dy = torch.from_numpy(w0.dy).to(dev)
+    lam = w0.l1_coeff
+    stack = SparseFFNStack(ws, l1_coeff=lam, cap=w0.cap, max_dense=1024, tensor_cores=True)
+    xs = x.clone().requires_grad_(True)
+
+    def ours():
+        xs.grad = None
+        for prm in stack.parameters():
+            prm.grad = None
+        (stack(xs) * dy).sum().backward()
+
+    dense_w = [[t.detach().clone().requires_grad_(True) for t in layer] for layer in ws]
+    xd = x.clone().requires_grad_(True)
+
+    def dense():
+        xd.grad = None
+        loss = 0.0
+        h_sum = 0.0
+        S = xd.float()
+        for Wg, Wu, Wd in dense_w:
+            for t in (Wg, Wu, Wd):
+                t.grad = None
+            X = S.to(torch.bfloat16)
+            hh = torch.relu(X @ Wg.t())
+            y = (hh * (X @ Wu.t())) @ Wd
+            y = torch.cat([y[:, :-1], torch.zeros_like(y[:, -1:])], dim=1)
+            h_sum = h_sum + hh.sum(dtype=torch.float32)
+            S = S + y.float()
+        loss = (S * dy).sum() + lam * h_sum
+        loss.backward()
+
+    K = max(2, args.train_steps)
+    t_ours = _timed(ours, flush, stream, 2, K)
+    flags = stack.status_flags()
+    if flags:
+        raise RuntimeError(f"device status flags {flags} in the stack")
+    t_dense = _timed(dense, flush, stream, 2, K)
+    n = int(os.environ.get("WORLD_SIZE", "1"))
+    return {
+        "metric": "FFN-stack training step (fwd+bwd through torch.autograd) tokens/s",
+        "layers": layers, "workload": w0.name + f", {layers} residual layers",
+        "ours": {"ms_per_step": t_ours, "tokens_per_s": job_tokens_per_s(w0.T, n, t_ours),
+                 "path": "SparseFFNStack (tensor-core hybrid via the C-ABI; fp32 residual "
+                         "stream and master weights, bf16 layer inputs)"},
+        "dense_context": {"ms_per_step": t_dense,
+                          "tokens_per_s": job_tokens_per_s(w0.T, n, t_dense),
+                          "path": "torch bf16 autograd (cuBLAS), same stack (fp32 residual "
+                                  "stream, bf16 weights and layer inputs)"},
+        "ratio": t_dense / t_ours,
     }
 
 
@@ -547,6 +662,17 @@ def run_ours(args, w):
                 "hbm": {"achieved": k2_gbs, "peak": hbm, "unit": "GB/s", "frac": k2_gbs / hbm,
                         "peak_source": f"{src} HBM copy"}}
     dense_ms = dense_context_forward(x, Wg, Wu, Wd, flush, stream, 3, K)
+    energy = None
+    if not args.no_energy:
+        e_ours = energy_per_token(step, w.T, stream, local)
+        e_dense = energy_per_token(
+            lambda: (torch.relu(x @ Wg.t()) * (x @ Wu.t())) @ Wd, w.T, stream, local)
+        if e_ours and e_dense:
+            energy = {"ours": e_ours, "dense_context": e_dense,
+                      "ratio": e_ours["joules_per_token"] / e_dense["joules_per_token"],
+                      "how": ("board power (nvidia-smi power.draw, 100 ms samples, idle power "
+                              "included) x CUDA-event time of ~1.5 s of back-to-back steps, "
+                              "no L2 flush, per token")}
 
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
@@ -568,11 +694,14 @@ def run_ours(args, w):
         "dense_context": {
             "ms_per_step": dense_ms, "tokens_per_s": job_tokens_per_s(w.T, ws, dense_ms),
             "what": "torch bf16 dense gated FFN (cuBLAS), all neurons, context only"},
+        "energy": energy,
         "clocks": clk_sum,
     }
     if not args.no_train:
         out["train"] = run_train(args, dev, flush, stream)
         out["train"]["n_gpus"] = ws
+        if not args.no_stack:
+            out["train"]["stack"] = run_stack(args, dev, flush, stream)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, n, s = time_oracle(w, budget_s=args.ref_budget)
         out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
@@ -597,6 +726,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-train", action="store_true", help="skip the training-step section")
     ap.add_argument("--train-steps", type=int, default=5)
+    ap.add_argument("--no-energy", action="store_true", help="skip the energy-per-token section")
+    ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack section")
     ap.add_argument("--no-flush", action="store_true",
                     help="skip the L2 flush (profiling runs only; not a valid bench number)")
     args = ap.parse_args()

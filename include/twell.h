@@ -258,9 +258,9 @@ twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, const float* u
  *   tiles X_ell W_u and dY_ell W_d^T of which only the ELL entries are kept;
  *   sparse-to-dense products (y, dx, dW_g^T, dW_u^T, dW_d) expand the ELL
  *   values tile by tile in shared memory into bf16 operands.
- * The sparse values h u and du enter the tensor cores rounded to bf16
- * (relative error up to 2^-8 each), as do dz and dy in the weight
- * gradients; dy in da and dz in dx are split into bf16 hi and lo halves.
+ * The sparse values h u (in y) and du enter the tensor cores rounded to bf16
+ * (relative error up to 2^-8 each); dy (in da and dW_d), dz (in dx and
+ * dW_g) and h u (in dW_d) are split into bf16 hi and lo halves.
  * Accumulation is fp32; results differ from the CUDA-core entry points by
  * that rounding.  Requires
  * D % 64 == 0 and C in {16, 32}; other shapes return TWELL_ERR_UNSUPPORTED.

@@ -406,3 +406,49 @@ def training_loss(X, G, U, Dn, dY, l1_coeff):
     y = ffn_forward_f64(X, G, U, Dn)
     z = X @ G.T
     return float(np.sum(y * dY) + l1_coeff * np.sum(np.where(z > 0, z, 0.0)))
+
+
+def stack_forward_backward(x, layers, dy, l1_coeff, bias_feature=True, round_inputs=True,
+                           inputs=None, actives=None):
+    """A residual stack of gated FFN layers, x_{l+1} = x_l + y_l with
+    y_l = FFN_l(a_l), and the gradients of
+    L = sum(x_L * dy) + l1_coeff * sum_l sum(h_l).
+
+    ``x`` bf16 bits [T][D]; ``layers`` a list of (Wg_t, Wu_t, Wd) bf16 bits.
+    The stream x_l is kept in fp64; each layer's input a_l is x_l rounded to
+    bf16 (``round_inputs``), or the bf16 bits ``inputs[l]`` when given; with
+    ``bias_feature`` the last feature of y_l is dropped (feature D - 1 stays
+    the constant gate-threshold input).  ``actives`` (boolean [T][F] per
+    layer) optionally replaces the z > 0 decisions, so a ReLU kink that two
+    computations straddle does not make their gradients differ by O(1).
+    The backward treats the rounding of a_l as the identity and chains the
+    single-layer gradients of ``ffn_backward_f64`` in reverse order:
+    dL/dx_l = dL/dx_{l+1} + dx(layer l, dy = dL/dx_{l+1} without the bias
+    feature).  Returns (x_L [T][D] fp64, dL/dx_0, [(dWg_t, dWu_t, dWd)])."""
+    X = bf16_to_f64(x)
+    ws = [tuple(bf16_to_f64(w) for w in layer) for layer in layers]
+    As = []
+    for i, (G, U, Dn) in enumerate(ws):
+        if inputs is not None:
+            A = bf16_to_f64(inputs[i])
+        elif round_inputs:
+            A = bf16_to_f64(f32_to_bf16(X.astype(np.float32)))
+        else:
+            A = X
+        As.append(A)
+        y = ffn_forward_f64(A, G, U, Dn, None if actives is None else actives[i])
+        if bias_feature:
+            y[:, -1] = 0.0
+        X = X + y
+    g = np.asarray(dy, dtype=np.float64).copy()
+    grads = [None] * len(ws)
+    for i in range(len(ws) - 1, -1, -1):
+        G, U, Dn = ws[i]
+        dyl = g.copy()
+        if bias_feature:
+            dyl[:, -1] = 0.0
+        dx, dg, du, dd = ffn_backward_f64(As[i], G, U, Dn, dyl, l1_coeff,
+                                          None if actives is None else actives[i])
+        grads[i] = (dg, du, dd)
+        g = g + dx
+    return X, g, grads

@@ -91,3 +91,51 @@ def test_inactive_entries_get_no_gradient():
     assert len(dead) > 0
     _, dg, du, dd = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, w.dy, 0.5)
     assert not dg[dead].any() and not du[dead].any() and not dd[dead].any()
+
+
+def test_stack_chain_rule_finite_differences():
+    # two residual layers without stream rounding: the chained gradients of
+    # stack_forward_backward match central differences of the stack's loss
+    rng = np.random.default_rng(21)
+    T, D, F = 3, 8, 16
+
+    def bits(a):
+        return oracle.f32_to_bf16(a.astype(np.float32))
+
+    x = bits(rng.standard_normal((T, D)))
+    layers = [tuple(bits(rng.standard_normal((F, D)) * 0.4) for _ in range(3)) for _ in range(2)]
+    dy = rng.standard_normal((T, D))
+    lam = 0.05
+    out, dx0, grads = oracle.stack_forward_backward(x, layers, dy, lam, round_inputs=False)
+    ws = [[oracle.bf16_to_f64(w) for w in layer] for layer in layers]
+
+    def loss(X0, ws):
+        X = X0
+        total = 0.0
+        for G, U, Dn in ws:
+            z = X @ G.T
+            total += lam * np.sum(np.where(z > 0, z, 0.0))
+            y = oracle.ffn_forward_f64(X, G, U, Dn)
+            y[:, -1] = 0.0
+            X = X + y
+        return total + float(np.sum(X * dy))
+
+    X0 = oracle.bf16_to_f64(x)
+    eps = 1e-6
+    for (t, d) in [(0, 0), (1, 3), (2, 7)]:
+        Xp, Xm = X0.copy(), X0.copy()
+        Xp[t, d] += eps
+        Xm[t, d] -= eps
+        fd = (loss(Xp, ws) - loss(Xm, ws)) / (2 * eps)
+        assert abs(fd - dx0[t, d]) <= 1e-5 * max(1.0, abs(fd))
+    for l in range(2):
+        for k in range(3):
+            for (j, d) in [(0, 0), (5, 2), (15, 7)]:
+                wp = [list(w) for w in ws]
+                wm = [list(w) for w in ws]
+                wp[l][k] = ws[l][k].copy()
+                wm[l][k] = ws[l][k].copy()
+                wp[l][k][j, d] += eps
+                wm[l][k][j, d] -= eps
+                fd = (loss(X0, wp) - loss(X0, wm)) / (2 * eps)
+                assert abs(fd - grads[l][k][j, d]) <= 1e-5 * max(1.0, abs(fd)), (l, k, j, d)
