@@ -11,8 +11,13 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread): 128 x BN x 16
 //               bf16 MMAs accumulating fp32 in TMEM, two accumulator buffers
 //   warps 2..5  epilogue: each thread owns one output row of the 128-row
-//               tile, reads its fp32 z from TMEM (tcgen05.ld 32x32b) and
-//               packs every 128-column slice straight into TwELL.
+//               tile, reads its 128 fp32 z of a slice from TMEM at once
+//               (four tcgen05.ld 32x32b), and packs the slice straight into
+//               TwELL: a 32-bit mask of z > 0 per 32-column chunk, a walk over
+//               its set bits (ascending columns), the chunk staged in a
+//               private shared-memory row (XOR-swizzled by 16-byte chunk) only
+//               when it has entries; spilled slices are written from the
+//               registers already loaded.
 // The accumulator is double-buffered so the epilogue of tile i overlaps the
 // MMAs of tile i+1.
 #include "common.cuh"
@@ -47,7 +52,8 @@ struct GateCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int STAGING = 128 * 128;  // a 32-column chunk per epilogue thread
+  static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + BAR_BYTES + 1024;
 };
 
 __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
@@ -64,7 +70,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * Cfg::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -101,8 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-        const int m_blk = tile % p.num_m;
-        const int n_blk = tile / p.num_m;
+        const int m_blk = tile / p.num_n;
+        const int n_blk = tile % p.num_n;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
             flag(p.status, TWELL_FLAG_TIMEOUT);
@@ -167,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int W = p.W;
     int local = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
-      const int m_blk = tile % p.num_m;
-      const int n_blk = tile / p.num_m;
+      const int m_blk = tile / p.num_n;
+      const int n_blk = tile % p.num_n;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       // the decision must be warp-uniform: tcgen05.ld below is warp-collective
@@ -179,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int t = m_blk * BM + row;
       const bool valid = t < p.T;
+      uint8_t* my_stage = staging + row * 128;
 #pragma unroll 1
       for (int sub = 0; sub < BN / TWELL_TILE; ++sub) {
         const int kt = n_blk * (BN / TWELL_TILE) + sub;
@@ -188,68 +196,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t rt = static_cast<size_t>(valid ? t : 0) * p.n_t + kt;
         float* vrow = p.val + rt * W;
         uint8_t* crow = p.col + rt * W;
+        uint32_t r[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r[ch]);
+        ptx::tmem_wait_ld();
         int c = 0;
-#pragma unroll 1
-        for (int ch = 0; ch < TWELL_TILE / 32; ++ch) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r);
-          ptx::tmem_wait_ld();
-          if (valid) {
-            if (p.z_debug) {
-              float4* zd = reinterpret_cast<float4*>(
-                  p.z_debug + static_cast<size_t>(t) * p.F + kt * TWELL_TILE + ch * 32);
+        if (valid) {
+          if (p.z_debug) {
+            float4* zd = reinterpret_cast<float4*>(p.z_debug + static_cast<size_t>(t) * p.F +
+                                                   kt * TWELL_TILE);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                zd[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                    __uint_as_float(r[4 * i + 2]),
-                                    __uint_as_float(r[4 * i + 3]));
-            }
+                zd[ch * 8 + i] = make_float4(
+                    __uint_as_float(r[ch][4 * i]), __uint_as_float(r[ch][4 * i + 1]),
+                    __uint_as_float(r[ch][4 * i + 2]), __uint_as_float(r[ch][4 * i + 3]));
+          }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float v = __uint_as_float(r[i]);
-              if (v > 0.0f) {
-                if (c < W) {
-                  vrow[c] = v;
-                  crow[c] = static_cast<uint8_t>(ch * 32 + i);
-                }
-                ++c;
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (__uint_as_float(r[ch][i]) > 0.0f) m |= 1u << i;
+            if (m == 0u) continue;
+            const int n = __popc(m);
+            if (c < W) {
+              // stage the chunk, then store its actives in column order
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(my_stage + ((j ^ (row & 7)) << 4)) =
+                    make_uint4(r[ch][4 * j], r[ch][4 * j + 1], r[ch][4 * j + 2],
+                               r[ch][4 * j + 3]);
+              uint32_t mm = m;
+              for (int e = c; e < W && mm != 0u; ++e) {
+                const int i = __ffs(mm) - 1;
+                mm &= mm - 1u;
+                vrow[e] = *reinterpret_cast<const float*>(
+                    my_stage + ((((i >> 2) ^ (row & 7)) << 4) | ((i & 3) << 2)));
+                crow[e] = static_cast<uint8_t>(ch * 32 + i);
               }
             }
+            c += n;
           }
+          p.cnt[rt] = static_cast<uint8_t>(c);
         }
         const bool spill = valid && c > W;
-        if (valid) p.cnt[rt] = static_cast<uint8_t>(c);
-        if (__any_sync(0xffffffffu, spill)) {
-          int slot = -1;
-          if (spill) {
-            slot = atomicAdd(p.spill_n, 1);
-            p.spill_slot[rt] = slot;
-            if (slot < p.spill_cap) {
-              p.spill_rt[slot] = static_cast<int32_t>(rt);
-            } else {
-              flag(p.status, TWELL_FLAG_SPILL_FULL);
-              slot = -1;
-            }
-          }
-#pragma unroll 1
-          for (int ch = 0; ch < TWELL_TILE / 32; ++ch) {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r);
-            ptx::tmem_wait_ld();
-            if (slot >= 0) {
-              float4* dst = reinterpret_cast<float4*>(
-                  p.spill_val + static_cast<size_t>(slot) * TWELL_TILE + ch * 32);
+        if (spill) {
+          const int slot = atomicAdd(p.spill_n, 1);
+          p.spill_slot[rt] = slot;
+          if (slot < p.spill_cap) {
+            p.spill_rt[slot] = static_cast<int32_t>(rt);
+            float4* dst = reinterpret_cast<float4*>(p.spill_val +
+                                                    static_cast<size_t>(slot) * TWELL_TILE);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 float e[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const float v = __uint_as_float(r[4 * i + k]);
+                  const float v = __uint_as_float(r[ch][4 * i + k]);
                   e[k] = v > 0.0f ? v : 0.0f;
                 }
-                dst[i] = make_float4(e[0], e[1], e[2], e[3]);
+                dst[ch * 8 + i] = make_float4(e[0], e[1], e[2], e[3]);
               }
-            }
+          } else {
+            flag(p.status, TWELL_FLAG_SPILL_FULL);
           }
         }
       }
