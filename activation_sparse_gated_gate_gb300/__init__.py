@@ -18,6 +18,7 @@ import torch
 
 __all__ = [
     "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
+    "twell_ffn_fwd_tc",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd",
     "twell_status_string",
@@ -41,6 +42,7 @@ class TwellStruct(ctypes.Structure):
         ("T", c_i32), ("F", c_i32), ("tile", c_i32), ("width", c_i32),
         ("val", c_ptr), ("col", c_ptr), ("cnt", c_ptr), ("spill_slot", c_ptr),
         ("spill_cap", c_i32), ("spill_n", c_ptr), ("spill_rt", c_ptr), ("spill_val", c_ptr),
+        ("block_bits", c_ptr),
     ]
 
 
@@ -68,6 +70,8 @@ _SIGNATURES = {
                                 c_ptr, c_ptr, c_ptr]),
     "twell_ffn_fwd": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
                               c_ptr, c_ptr]),
+    "twell_ffn_fwd_tc": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
+                                 c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "twell_to_hybrid": (c_i32, [ctypes.POINTER(TwellStruct), ctypes.POINTER(HybridStruct),
                                 c_ptr, c_ptr]),
     "twell_workspace_size": (ctypes.c_size_t, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
@@ -139,10 +143,12 @@ class TwELL:
 
     ``spill_cap`` defaults to T * n_t slices, enough for every (row, tile)
     to overflow.  ``status`` is a device int32 the kernels OR flags into.
+    ``block_bits`` (default on) adds the per-block union bitmap that the
+    gate kernel fills and the tensor-core forward reads.
     """
 
     def __init__(self, T: int, F: int, width: int, spill_cap: int | None = None,
-                 device=None, tile: int = TILE):
+                 device=None, tile: int = TILE, block_bits: bool = True):
         device = torch.device(device if device is not None else "cuda")
         n_t = F // tile
         if spill_cap is None:
@@ -159,10 +165,13 @@ class TwELL:
         self.spill_val = torch.empty((max(spill_cap, 1), tile), dtype=torch.float32,
                                      device=device)
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+        self.block_bits = (torch.zeros(((T + 127) // 128, F // 32), dtype=torch.int32,
+                                       device=device) if block_bits else None)
         self.struct = TwellStruct(
             T, F, tile, width, self.val.data_ptr(), self.col.data_ptr(), self.cnt.data_ptr(),
             self.spill_slot.data_ptr(), spill_cap, self.spill_n.data_ptr(),
-            self.spill_rt.data_ptr(), self.spill_val.data_ptr())
+            self.spill_rt.data_ptr(), self.spill_val.data_ptr(),
+            self.block_bits.data_ptr() if block_bits else None)
 
 
 def twell_gate_pack(x, Wg_t, out: TwELL, z_debug=None, status=None, stream=None):
@@ -201,6 +210,32 @@ def twell_ffn_fwd(x, h: TwELL, Wu_t, Wd, y=None, status=None, stream=None):
         _check(lib().twell_ffn_fwd(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
                                    _ptr(y), _ptr(status), _stream(stream)),
                "twell_ffn_fwd")
+    return y
+
+
+def twell_ffn_fwd_tc(x, h: TwELL, Wu_t, Wd, y=None, ws=None, status=None, stream=None):
+    """Tensor-core (union-gather) up + down projection from the TwELL gate
+    ``h``: the same function as ``twell_ffn_fwd`` with h*u rounded to bf16;
+    returns y [T][D] fp32 (allocated if not given).  ``ws`` is the device
+    workspace (allocated if not given)."""
+    _need(x, torch.bfloat16, "x")
+    _need(Wu_t, torch.bfloat16, "Wu_t")
+    _need(Wd, torch.bfloat16, "Wd")
+    T, D = x.shape
+    if y is None:
+        y = torch.empty((T, D), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, "y")
+    if Wu_t.shape != (h.F, D) or Wd.shape != (h.F, D) or T != h.T:
+        raise ValueError("shape mismatch: x [T][D], Wu_t and Wd [F][D]")
+    nbytes = twell_workspace_size(WS_FFN_FWD_TC, T, D, h.F, 0, 0)
+    if ws is None:
+        ws = _workspace(nbytes, x.device)
+    status = h.status if status is None else status
+    with torch.cuda.device(x.device):
+        _check(lib().twell_ffn_fwd_tc(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
+                                      _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _ptr(status), _stream(stream)),
+               "twell_ffn_fwd_tc")
     return y
 
 
@@ -255,6 +290,7 @@ WS_HYBRID_FWD = 1
 WS_HYBRID_BWD = 2
 WS_HYBRID_FWD_TC = 3
 WS_HYBRID_BWD_TC = 4
+WS_FFN_FWD_TC = 5
 
 
 def twell_workspace_size(op: int, T: int, D: int, F: int, cap: int, max_dense: int) -> int:

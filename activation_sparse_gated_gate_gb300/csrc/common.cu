@@ -74,7 +74,7 @@ twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
 twell_status make_tmap_2d(CUtensorMap* map, int elem_bytes, const void* base, uint64_t inner,
                           uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                           uint64_t pitch_bytes, int swizzle) {
-  if (elem_bytes != 1 && elem_bytes != 2) return TWELL_ERR_INVALID;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return TWELL_ERR_INVALID;
   CUtensorMapSwizzle sw;
   switch (swizzle) {
     case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
@@ -99,7 +99,11 @@ twell_status make_tmap_2d(CUtensorMap* map, int elem_bytes, const void* base, ui
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(
-      map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+      map,
+      elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+      : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                        : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+      2,
       const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TWELL_OK : TWELL_ERR_INVALID;

@@ -41,7 +41,7 @@ twell_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
                                uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                                uint64_t pitch = 0);
 
-// 2-D tensor map of 1-byte (u8) or 2-byte (bf16) elements over a row-major
+// 2-D tensor map of 1-byte (u8), 2-byte (bf16) or 4-byte (fp32) elements over a row-major
 // [outer][inner] array with rows `pitch_bytes` apart (a multiple of 16), box
 // [box_outer][box_inner], zero fill out of bounds.  `swizzle` = 0 (none) or
 // the span in bytes (32, 64, 128): in shared memory, the 16-byte chunk index

@@ -1,0 +1,804 @@
+// Tensor-core (union-gather) variant of the fused up + down projection from
+// a TwELL gate ("Sparser, Faster, Lighter Transformer Language Models",
+// section 2.B.2: the up and down projections are computed only for the
+// gate's active neurons, with the kernels built to keep the tensor cores
+// busy).
+//
+// The rows of a block of 128 tokens share one gathered operand: the union U
+// of their active neurons (ascending).  The forward is then two dense
+// tcgen05 GEMMs over that union alone:
+//   up    u = x_blk . W_u[:, U]          (128 x |U|, K = D), and in the
+//         epilogue a = bf16(h u) at each row's own active neurons, 0 at the
+//         other union positions, written to a [T][Fp] bf16 scratch matrix in
+//         union-position order
+//   down  y_blk = a_blk . W_d[U, :]      (128 x D, K = |U|), fp32 out
+// The union's weight rows are gathered into the 128-byte-swizzled operand
+// tiles by four warps with 16-byte cp.async copies (each copy lands where a
+// TMA box with that swizzle would put it); the token tiles (x, a) come by
+// TMA.  The union bitmap of each block comes from the gate kernel (TwELL
+// block_bits) or, without it, from a small kernel over the TwELL; a scan
+// kernel turns it into U (padded with neuron 0 to a multiple of 256), the
+// per-word position prefix and the list of (block, 256-position chunk) units
+// of the up GEMM.  The up epilogue finds its row's entries in the chunk from
+// the TwELL itself while the chunk's MMAs run.
+//
+// Both GEMMs: one persistent CTA per SM, tiles of 128 x 256 outputs, K in
+// blocks of 64, four shared-memory stages [A 16 KB][B 32 KB]:
+//   warp 0      TMA producer of the A tiles
+//   warp 1      TMEM allocation (two 256-column accumulators) and MMA issue
+//   warps 2-5   epilogue, one TMEM lane quarter each
+//   warps 6-13  B gather: four groups of two warps, group g filling stage g
+//               (32 copies per thread), marking it full once its copies
+//               have landed and it has fenced them to the async proxy
+// Every wait is bounded (about a second); a wait that runs out sets
+// TWELL_FLAG_TIMEOUT and the CTA leaves its loops, frees its TMEM and exits.
+#include <cuda_bf16.h>
+
+#include "fused.cuh"
+#include "ptx.cuh"
+#include "tc_ell.cuh"
+
+namespace twell {
+namespace {
+
+constexpr int UG_BM = 128;
+constexpr int UG_BN = 256;
+constexpr int UG_BK = 64;
+constexpr int UG_ST = 4;
+constexpr int UG_A = UG_BM * UG_BK * 2;
+constexpr int UG_B = UG_BN * UG_BK * 2;
+constexpr int UG_STAGE = UG_A + UG_B;
+constexpr int UG_GROUP = 64;            // threads of a gather group (one per stage)
+constexpr int UG_GATHER0 = 192;         // first thread of the gather groups
+constexpr int UG_THREADS = UG_GATHER0 + UG_ST * UG_GROUP;
+constexpr int UG_HSLOTS = 32;           // up epilogue: gate values staged per row
+
+// Shared memory: [stages][output staging: 4 warps x 2 buffers of a 32 x 32
+// chunk][barriers 256 B][up: gate-value slots 128 x UG_HSLOTS fp32]
+template <int MODE>
+struct UgSmem {
+  static constexpr int STG_BUF = MODE == 0 ? 32 * 32 * 2 : 32 * 32 * 4;
+  static constexpr int STG = UG_ST * UG_STAGE;
+  static constexpr int BARS = STG + 8 * STG_BUF;
+  static constexpr int SLOTS = BARS + 256;
+  static constexpr int BYTES = SLOTS + (MODE == 0 ? UG_BM * UG_HSLOTS * 4 : 0) + 1024;
+};
+constexpr int UG_PREP_THREADS = 256;
+constexpr int UG_ROWS_PER_CTA = 16;     // preparation: rows per CTA
+constexpr int UG_MAX_F = 32768;         // bitmap words <= 4 per preparation thread
+
+enum { UG_UP = 0, UG_DOWN = 1 };
+
+struct UgArgs {
+  // TwELL gate
+  const float* val;
+  const uint8_t* col;
+  const uint8_t* cnt;
+  const int32_t* spill_slot;
+  const float* spill_val;
+  int32_t spill_cap;
+  int32_t T, D, F, Fp, nw, n_t, W, n_m, nj, nN;
+  const uint16_t* Wu_t;
+  const uint16_t* Wd;
+  float* y;
+  // workspace
+  int32_t* ctr;     // [0]: units of the up GEMM
+  uint32_t* gbm;    // [n_m][gbm_pitch] union bitmap of each block (F / 32 words used)
+  int32_t gbm_pitch;
+  int32_t* nU;      // [n_m] union sizes
+  int32_t* Ulist;   // [n_m][Fp] union neurons, ascending, padded with 0
+  int32_t* units;   // [n_m * nj] up-GEMM units (block * nj + chunk)
+  int32_t* wpre;    // [n_m][nw] union position of each bitmap word's first bit
+  uint16_t* abuf;   // [T][Fp] a = bf16(h u) in union-position order
+  int32_t* status;
+};
+
+struct UgLayout {
+  size_t ctr, gbm, nU, Ulist, units, wpre, abuf, bytes;
+  int64_t Fp, nw, n_m, nj;
+};
+
+inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+UgLayout ug_layout(int64_t T, int64_t F) {
+  UgLayout L{};
+  L.Fp = (F + 255) / 256 * 256;
+  L.nw = L.Fp / 32;
+  L.n_m = (T + UG_BM - 1) / UG_BM;
+  L.nj = L.Fp / 256;
+  size_t o = 0;
+  L.ctr = o;
+  o += 256;
+  L.gbm = o;
+  o = up256(o + static_cast<size_t>(L.n_m) * L.nw * 4);
+  L.nU = o;
+  o = up256(o + L.n_m * 4);
+  L.Ulist = o;
+  o = up256(o + static_cast<size_t>(L.n_m) * L.Fp * 4);
+  L.units = o;
+  o = up256(o + static_cast<size_t>(L.n_m) * L.nj * 4);
+  L.wpre = o;
+  o = up256(o + static_cast<size_t>(L.n_m) * L.nw * 4);
+  L.abuf = o;
+  o = up256(o + static_cast<size_t>(T) * L.Fp * 2);
+  L.bytes = o;
+  return L;
+}
+
+// ------------------------------------------------------------ preparation
+//   ug_bits_kernel  (only for a TwELL without block_bits; grid: blocks x 8
+//                   CTAs of 16 rows) ORs every active neuron of its rows
+//                   into the block's union bitmap (shared memory, then global
+//                   atomics into the zeroed [n_m][nw] bitmap).
+//   ug_scan_kernel  (one CTA per block) takes the exclusive prefix of the
+//                   bitmap words' popcounts -- a neuron's union position is
+//                   the prefix of its word plus the set bits below it in the
+//                   word -- and writes it, U (ascending, padded with neuron
+//                   0), |U| and the block's up-GEMM units.
+// A (row, tile) whose spill slice is missing is skipped
+// (TWELL_FLAG_SPILL_FULL), as in the fused CUDA-core kernel.
+template <typename Fn>
+__device__ __forceinline__ void ug_walk_pair(const UgArgs& p, size_t rt, int k, bool flag_missing,
+                                             Fn&& fn) {
+  const int c = p.cnt[rt];
+  if (c == 0) return;
+  if (c <= p.W) {
+    const uint8_t* cp = p.col + rt * p.W;
+    const float* vp = p.val + rt * p.W;
+    for (int s = 0; s < c; ++s) fn(k * TWELL_TILE + cp[s], vp[s]);
+  } else {
+    const int sl = p.spill_slot[rt];
+    if (sl < 0 || sl >= p.spill_cap) {
+      if (flag_missing) atomicOr(p.status, TWELL_FLAG_SPILL_FULL);
+      return;
+    }
+    const float* sv = p.spill_val + static_cast<size_t>(sl) * TWELL_TILE;
+    for (int cc = 0; cc < TWELL_TILE; ++cc) {
+      const float v = sv[cc];
+      if (v > 0.0f) fn(k * TWELL_TILE + cc, v);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p) {
+  extern __shared__ uint32_t psm[];
+  const int nw = p.nw;
+  uint32_t* bm = psm;
+  const int m = blockIdx.x;
+  const int r0 = m * UG_BM + blockIdx.y * UG_ROWS_PER_CTA;
+  const int rows = min(UG_ROWS_PER_CTA, p.T - r0);
+  if (rows <= 0) return;
+  for (int i = threadIdx.x; i < nw; i += UG_PREP_THREADS) bm[i] = 0u;
+  __syncthreads();
+  const int n_t = p.n_t;
+  const size_t rt0 = static_cast<size_t>(r0) * n_t;  // the rows' (row, tile) pairs are contiguous
+  for (int q = threadIdx.x; q < rows * n_t; q += UG_PREP_THREADS)
+    ug_walk_pair(p, rt0 + q, q % n_t, true,
+                 [&](int n, float) { atomicOr(&bm[n >> 5], 1u << (n & 31)); });
+  __syncthreads();
+  uint32_t* g = p.gbm + static_cast<size_t>(m) * p.gbm_pitch;
+  for (int i = threadIdx.x; i < nw; i += UG_PREP_THREADS)
+    if (bm[i]) atomicOr(&g[i], bm[i]);
+}
+
+__global__ void __launch_bounds__(UG_PREP_THREADS) ug_scan_kernel(const UgArgs p) {
+  extern __shared__ uint32_t psm[];
+  const int nw = p.nw;
+  uint32_t* bm = psm;                            // [nw]
+  int* wpre = reinterpret_cast<int*>(psm + nw);  // [nw]
+  __shared__ int wsum[UG_PREP_THREADS / 32];
+  __shared__ int s_total, s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int m = blockIdx.x;
+  const uint32_t* g = p.gbm + static_cast<size_t>(m) * p.gbm_pitch;
+  for (int i = tid; i < nw; i += UG_PREP_THREADS) bm[i] = i < p.F / 32 ? g[i] : 0u;
+  __syncthreads();
+
+  // exclusive prefix of the words' popcounts, four words per thread
+  int c[4], v = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int w = 4 * tid + e;
+    c[e] = w < nw ? __popc(bm[w]) : 0;
+    v += c[e];
+  }
+  const int mine = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  if (lane == 31) wsum[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < UG_PREP_THREADS / 32 ? wsum[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, s, d);
+      if (lane >= d) s += o;
+    }
+    if (lane < UG_PREP_THREADS / 32) wsum[lane] = s;
+    if (lane == UG_PREP_THREADS / 32 - 1) s_total = s;
+  }
+  __syncthreads();
+  int ex = v - mine + (warp > 0 ? wsum[warp - 1] : 0);
+  int32_t* wg = p.wpre + static_cast<size_t>(m) * nw;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int w = 4 * tid + e;
+    if (w < nw) {
+      wpre[w] = ex;
+      wg[w] = ex;
+    }
+    ex += c[e];
+  }
+  const int nU = s_total;
+  const int chunks = (nU + 255) >> 8;
+  if (tid == 0) {
+    p.nU[m] = nU;
+    s_base = chunks > 0 ? atomicAdd(p.ctr, chunks) : 0;
+  }
+  __syncthreads();
+  int32_t* Ul = p.Ulist + static_cast<size_t>(m) * p.Fp;
+  for (int w = tid; w < nw; w += UG_PREP_THREADS) {
+    uint32_t bits = bm[w];
+    int r = wpre[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      Ul[r++] = 32 * w + b;
+    }
+  }
+  for (int i = nU + tid; i < chunks * 256; i += UG_PREP_THREADS) Ul[i] = 0;
+  for (int jn = tid; jn < chunks; jn += UG_PREP_THREADS) p.units[s_base + jn] = m * p.nj + jn;
+}
+
+// --------------------------------------------------------------- the GEMMs
+struct UgUnit {
+  int m, j, kb;  // token block, output chunk (up: union chunk; down: D tile), K blocks
+};
+
+template <int MODE>
+__device__ __forceinline__ UgUnit ug_unit(const UgArgs& p, int u) {
+  UgUnit r;
+  if (MODE == UG_UP) {
+    const int code = p.units[u];
+    r.m = code / p.nj;
+    r.j = code - r.m * p.nj;
+    r.kb = p.D / UG_BK;
+  } else {
+    r.m = u / p.nN;
+    r.j = u - r.m * p.nN;
+    r.kb = (p.nU[r.m] + UG_BK - 1) / UG_BK;
+  }
+  return r;
+}
+
+// v[i] for a run-time i in [0, 32) without indexing a register array: a
+// five-level select tree.
+__device__ __forceinline__ uint32_t select32(const uint32_t (&v)[32], int i) {
+  uint32_t a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a[k] = (i & 1) ? v[2 * k + 1] : v[2 * k];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) b[k] = (i & 2) ? a[2 * k + 1] : a[2 * k];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) c[k] = (i & 4) ? b[2 * k + 1] : b[2 * k];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) d[k] = (i & 8) ? c[2 * k + 1] : c[2 * k];
+  return (i & 16) ? d[1] : d[0];
+}
+
+// Entries (neuron, gate value) of the TwELL tiles [k0, k1] of the row whose
+// (row, tile) pairs start at rtb, in ascending neuron order, for width WV
+// (8 or 16): B tiles' counts, then all their slots (16-byte loads; slots past
+// the count are loaded, not used), are loaded before any entry is used.
+template <int WV, int B, typename Fn>
+__device__ __forceinline__ void walk_tiles(const UgArgs& p, size_t rtb, int k0, int k1, Fn&& fn) {
+  for (int k = k0; k <= k1; k += B) {
+    int cn[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) cn[b] = k + b <= k1 ? p.cnt[rtb + k + b] : 0;
+    uint32_t cw[B][WV / 4];
+    float vs[B][WV];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const size_t rt = rtb + k + b;
+      const bool in = cn[b] > 0 && cn[b] <= WV;
+      if (WV == 16) {
+        const uint4 c4 = in ? __ldg(reinterpret_cast<const uint4*>(p.col + rt * 16))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        cw[b][0] = c4.x;
+        cw[b][1] = c4.y;
+        cw[b][WV / 4 - 2] = c4.z;
+        cw[b][WV / 4 - 1] = c4.w;
+      } else {
+        const uint2 c2 =
+            in ? __ldg(reinterpret_cast<const uint2*>(p.col + rt * 8)) : make_uint2(0u, 0u);
+        cw[b][0] = c2.x;
+        cw[b][WV / 4 - 1] = c2.y;
+      }
+#pragma unroll
+      for (int g4 = 0; g4 < WV / 4; ++g4) {
+        const float4 v4 = in ? __ldg(reinterpret_cast<const float4*>(p.val + rt * WV) + g4)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        vs[b][4 * g4] = v4.x;
+        vs[b][4 * g4 + 1] = v4.y;
+        vs[b][4 * g4 + 2] = v4.z;
+        vs[b][4 * g4 + 3] = v4.w;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      if (cn[b] == 0) continue;
+      if (cn[b] > WV) {  // spilled: the slice's positive values
+        ug_walk_pair(p, rtb + k + b, k + b, false, fn);
+        continue;
+      }
+#pragma unroll
+      for (int e = 0; e < WV; ++e)
+        if (e < cn[b])
+          fn((k + b) * TWELL_TILE + static_cast<int>((cw[b][e >> 2] >> (8 * (e & 3))) & 0xffu),
+             vs[b][e]);
+    }
+  }
+}
+
+// Gate value of row t at neuron n read from the TwELL (0 if inactive or in a
+// missing spill slice): the slow path for rows with many entries in a chunk.
+__device__ __forceinline__ float twell_h_at(const UgArgs& p, int t, int n) {
+  const size_t rt = static_cast<size_t>(t) * p.n_t + (n >> 7);
+  const int col = n & (TWELL_TILE - 1);
+  const int c = p.cnt[rt];
+  if (c <= p.W) {
+    for (int s = 0; s < c; ++s)
+      if (p.col[rt * p.W + s] == col) return p.val[rt * p.W + s];
+    return 0.0f;
+  }
+  const int sl = p.spill_slot[rt];
+  if (sl < 0 || sl >= p.spill_cap) return 0.0f;
+  return p.spill_val[static_cast<size_t>(sl) * TWELL_TILE + col];
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(UG_THREADS, 1)
+    ug_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_out, const UgArgs p) {
+  using SM = UgSmem<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::BARS);
+  uint64_t* empty = full + UG_ST;
+  uint64_t* tfull = empty + UG_ST;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  float* hslots = reinterpret_cast<float*>(smem + SM::SLOTS);  // up: [128][UG_HSLOTS]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_units = MODE == UG_UP ? *p.ctr : p.n_m * p.nN;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < UG_ST; ++s) {
+      ptx::mbar_init(&full[s], 1 + UG_GROUP);  // the A producer's expect_tx + a gather group
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 128);
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 2 * UG_BN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------- TMA producer (A)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const UgUnit U = ug_unit<MODE>(p, u);
+        for (int kb = 0; kb < U.kb; ++kb) {
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
+            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            goto done;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], UG_A);
+          ptx::tma_load_2d(smem + stage * UG_STAGE, &map_a, &full[stage], kb * UG_BK,
+                           U.m * UG_BM);
+          if (++stage == UG_ST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(UG_BM, UG_BN, false, MODE == UG_DOWN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const UgUnit U = ug_unit<MODE>(p, u);
+        if (U.kb == 0) continue;
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        ++local;
+        if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
+          atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          goto done;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * UG_BN);
+        for (int kb = 0; kb < U.kb; ++kb) {
+          if (!ptx::mbar_wait(&full[stage], phase)) {
+            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            goto done;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(smem + stage * UG_STAGE);
+          const uint32_t b_addr = a_addr + UG_A;
+#pragma unroll
+          for (int kk = 0; kk < UG_BK / 16; ++kk) {
+            const uint64_t bd = MODE == UG_UP
+                                    ? ptx::sdesc_kmajor_sw128(b_addr + kk * 32)
+                                    : ptx::sdesc_mnmajor_sw128(b_addr + kk * 2048, 8192, 1024);
+            ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + kk * 32), bd, idesc,
+                          (kb | kk) ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[stage]);
+          if (++stage == UG_ST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        ptx::mma_commit(&tfull[acc]);
+      }
+    }
+  } else if (warp >= 6) {
+    // --------------------------------------------------------- B gather
+    // Group grp (64 threads) fills stage grp, i.e. the K blocks whose stage
+    // sequence number is grp mod 4: wait for the stage to be free, issue 32
+    // copies per thread, wait for them, fence them to the async proxy and
+    // arrive on the stage's full barrier.  The four groups keep all four
+    // stages in flight.
+    // up:   B = W_u^T rows of 256 union neurons x 64 K, K-major: neuron row
+    //       n at n * 128 bytes, its 16-byte chunk c at chunk c ^ (n & 7).
+    //       Thread g copies chunk g & 7 of rows (g >> 3) + 8 i.
+    // down: B = W_d rows of 64 union neurons (K) x 256 outputs, N-major in
+    //       four 64-column boxes of 8 KB: K row k of box b at b * 8192 +
+    //       k * 128, chunk c at chunk c ^ (k & 7).  Thread g copies chunk
+    //       g & 7 of box (g >> 3) & 3 of K rows (g >> 5) + 2 i; chunks past
+    //       D are zero-filled.
+    const int grp = (threadIdx.x - UG_GATHER0) / UG_GROUP;
+    const int g = (threadIdx.x - UG_GATHER0) % UG_GROUP;
+    const int cj = g & 7;
+    uint8_t* sBp = smem + grp * UG_STAGE + UG_A;
+    const uint32_t sB = ptx::smem_u32(sBp);
+    uint64_t* fb = &full[grp];
+    uint64_t* eb = &empty[grp];
+    int seq = 0;
+    int ids[32];
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const UgUnit U = ug_unit<MODE>(p, u);
+      if (U.kb == 0) continue;
+      const int32_t* Ul = p.Ulist + static_cast<size_t>(U.m) * p.Fp;
+      // first K block of this unit that is this group's
+      int kb = (grp - seq) & (UG_ST - 1);
+      const int seq0 = seq;
+      seq += U.kb;
+      if (kb >= U.kb) continue;
+      int col = 0;
+      uint32_t nbytes = 16;
+      if (MODE == UG_UP) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ids[i] = __ldg(Ul + U.j * 256 + (g >> 3) + 8 * i);
+      } else {
+        col = U.j * UG_BN + 64 * ((g >> 3) & 3) + 8 * cj;
+        nbytes = col < p.D ? 16u : 0u;
+        if (col >= p.D) col = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ids[i] = __ldg(Ul + kb * UG_BK + (g >> 5) + 2 * i);
+      }
+      for (; kb < U.kb; kb += UG_ST) {
+        const uint32_t phase = static_cast<uint32_t>((seq0 + kb) / UG_ST) & 1u;
+        if (!ptx::mbar_wait(eb, phase ^ 1u)) {
+          atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          goto done;
+        }
+        if (MODE == UG_UP) {
+          const uint32_t dst0 = sB + (g >> 3) * 128 + ((cj ^ (g >> 3)) << 4);
+          const size_t koff = static_cast<size_t>(kb) * UG_BK + 8 * cj;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ptx::cp_async16(dst0 + i * 1024, p.Wu_t + static_cast<size_t>(ids[i]) * p.D + koff);
+        } else {
+          const uint32_t box = sB + ((g >> 3) & 3) * 8192;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int k = (g >> 5) + 2 * i;
+            ptx::cp_async16(box + k * 128 + ((cj ^ (k & 7)) << 4),
+                            p.Wd + static_cast<size_t>(ids[i]) * p.D + col, nbytes);
+          }
+          if (kb + UG_ST < U.kb) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              ids[i] = __ldg(Ul + (kb + UG_ST) * UG_BK + (g >> 5) + 2 * i);
+          }
+        }
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<0>();
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(fb);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int local = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const UgUnit U = ug_unit<MODE>(p, u);
+      const int t = U.m * UG_BM + r;
+      const bool valid = t < p.T;
+      if (MODE == UG_DOWN && U.kb == 0) {  // no active neuron in the block: y rows are zero
+        if (valid) {
+          float* o = p.y + static_cast<size_t>(t) * p.D + U.j * UG_BN;
+          for (int n = 0; n < UG_BN && U.j * UG_BN + n < p.D; n += 4)
+            *reinterpret_cast<float4*>(o + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      ++local;
+      // Up: the row's active positions in the chunk (positions 256 j ..
+      // 256 j + 255 of U, i.e. neurons U[256 j] .. U[last]) as eight mask
+      // words, and the gate values of the first UG_HSLOTS of them (ascending)
+      // in the row's shared-memory slots.  They come from the row's TwELL
+      // tiles that cover those neurons, four tiles' counts and slots loaded
+      // at a time, while the chunk's MMAs run.
+      uint32_t mq[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      float* myslot = hslots + r * UG_HSLOTS;
+      const int32_t* Ul = p.Ulist + static_cast<size_t>(U.m) * p.Fp;
+      const int p0 = 256 * U.j;
+      if (MODE == UG_UP && valid) {
+        const int nUm = __ldg(p.nU + U.m);
+        const int lo_n = __ldg(Ul + p0);
+        const int hi_n = __ldg(Ul + min(p0 + 255, nUm - 1));
+        const uint32_t* bmr = p.gbm + static_cast<size_t>(U.m) * p.gbm_pitch;
+        const int32_t* wpr = p.wpre + static_cast<size_t>(U.m) * p.nw;
+        int nset = 0;
+        auto add = [&](int n, float h) {
+          if (n < lo_n || n > hi_n) return;
+          const int w = n >> 5;
+          const int pos =
+              __ldg(wpr + w) + __popc(__ldg(bmr + w) & ((1u << (n & 31)) - 1u)) - p0;
+          const uint32_t bit = 1u << (pos & 31);
+          const uint32_t wsel = pos >> 5;  // a select per word, not an index
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mq[k] |= (wsel == static_cast<uint32_t>(k) ? bit : 0u);
+          if (nset < UG_HSLOTS) myslot[nset] = h;
+          ++nset;
+        };
+        const size_t rtb = static_cast<size_t>(t) * p.n_t;
+        const int k0 = lo_n >> 7, k1 = hi_n >> 7;
+        if (p.W == 8) {
+          walk_tiles<8, 4>(p, rtb, k0, k1, add);
+        } else if (p.W == 16) {
+          walk_tiles<16, 2>(p, rtb, k0, k1, add);
+        } else {
+          for (int k = k0; k <= k1; ++k) ug_walk_pair(p, rtb + k, k, false, add);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
+        if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+        goto done;
+      }
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * UG_BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      // Output chunks of 32 columns go through a per-warp staging buffer
+      // (two per warp, alternating): each lane writes its row with the
+      // swizzle of the output tensor map (16-byte chunk j of row r at chunk
+      // j ^ (address bits 7..)), conflict-free, and lane 0 stores the warp's
+      // 32 x 32 box with one TMA store (rows past T are clipped).
+      const int row0 = U.m * UG_BM + q * 32;
+      if (MODE == UG_UP) {
+        int rank = 0;  // active positions of the row consumed so far
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+          ptx::tmem_wait_ld();
+          if (c == 7) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[acc]);
+          }
+          uint32_t mc = mq[0];
+#pragma unroll
+          for (int i = 0; i < 7; ++i) mq[i] = mq[i + 1];
+          // 64-byte rows, 64-byte swizzle: chunk j of row lane at j ^ ((lane >> 1) & 3).
+          // The row is zeroed, then each active position gets its bf16 a;
+          // the loop runs as often as the busiest lane of the warp needs.
+          uint8_t* buf = smem + SM::STG + (q * 2 + (c & 1)) * SM::STG_BUF;
+          if (lane == 0) ptx::bulk_wait_read<1>();
+          __syncwarp();
+          uint8_t* my_row = buf + lane * 64;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(my_row + 16 * j) = make_uint4(0u, 0u, 0u, 0u);
+          const int sw = (lane >> 1) & 3;
+          while (__any_sync(0xffffffffu, mc != 0u)) {
+            if (mc != 0u) {
+              const int i = __ffs(mc) - 1;
+              mc &= mc - 1u;
+              const float hv = rank < UG_HSLOTS
+                                   ? myslot[rank]
+                                   : twell_h_at(p, t, __ldg(Ul + p0 + 32 * c + i));
+              ++rank;
+              const float a = hv * __uint_as_float(select32(v, i));
+              *reinterpret_cast<uint16_t*>(my_row + ((((i >> 3) ^ sw)) << 4) + (i & 7) * 2) =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(a));
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&map_out, buf, 256 * U.j + 32 * c, row0);
+            ptx::bulk_commit();
+          }
+        }
+      } else {
+        const int nch = min(UG_BN, p.D - U.j * UG_BN) / 32;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+          ptx::tmem_wait_ld();
+          if (c == nch - 1) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[acc]);
+          }
+          // 128-byte rows, 128-byte swizzle: chunk j of row lane at j ^ (lane & 7)
+          uint8_t* buf = smem + SM::STG + (q * 2 + (c & 1)) * SM::STG_BUF;
+          if (lane == 0) ptx::bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&map_out, buf, U.j * UG_BN + 32 * c, row0);
+            ptx::bulk_commit();
+          }
+        }
+      }
+    }
+  }
+
+done:
+  // the epilogue's TMA stores have finished before the CTA's shared memory goes away
+  if (warp >= 2 && warp < 6 && lane == 0) ptx::bulk_wait_all();
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 2 * UG_BN);
+  }
+}
+
+template <int MODE>
+twell_status ug_launch(const CUtensorMap& map, const CUtensorMap& map_out, const UgArgs& a,
+                       int max_units, const DeviceInfo& dev, cudaStream_t s) {
+  constexpr int SMEM = UgSmem<MODE>::BYTES;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  auto kern = ug_gemm_kernel<MODE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
+      cudaSuccess)
+    return TWELL_ERR_CUDA;
+  if (max_units <= 0) return TWELL_OK;
+  const int grid = max_units < dev.sm_count ? max_units : dev.sm_count;
+  kern<<<grid, UG_THREADS, SMEM, s>>>(map, map_out, a);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t ffn_tc_workspace_bytes(int64_t T, int64_t F) { return ug_layout(T, F).bytes; }
+
+}  // namespace twell
+
+extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
+                                         const uint16_t* Wu_t, const uint16_t* Wd, int32_t D,
+                                         float* y, void* ws, size_t ws_bytes,
+                                         int32_t* status_dev, void* stream) {
+  using namespace twell;
+  if (h == nullptr) return TWELL_ERR_INVALID;
+  const int32_t T = h->T, F = h->F;
+  if (T < 0 || F <= 0 || F % TWELL_TILE != 0 || D <= 0 || D % UG_BK != 0)
+    return TWELL_ERR_INVALID;
+  if (F > UG_MAX_F) return TWELL_ERR_UNSUPPORTED;
+  twell_status st = check_twell(h, T, F, false);
+  if (st != TWELL_OK) return st;
+  if (T == 0) return TWELL_OK;
+  if (!x || !Wu_t || !Wd || !y || !status_dev || !ws) return TWELL_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return TWELL_ERR_INVALID;
+  const UgLayout L = ug_layout(T, F);
+  if (ws_bytes < L.bytes) return TWELL_ERR_INVALID;
+  DeviceInfo dev;
+  if ((st = require_sm103(&dev)) != TWELL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  UgArgs a{};
+  a.val = h->val;
+  a.col = h->col;
+  a.cnt = h->cnt;
+  a.spill_slot = h->spill_slot;
+  a.spill_val = h->spill_val;
+  a.spill_cap = h->spill_cap;
+  a.T = T;
+  a.D = D;
+  a.F = F;
+  a.Fp = static_cast<int32_t>(L.Fp);
+  a.nw = static_cast<int32_t>(L.nw);
+  a.n_t = F / TWELL_TILE;
+  a.W = h->width;
+  a.n_m = static_cast<int32_t>(L.n_m);
+  a.nj = static_cast<int32_t>(L.nj);
+  a.nN = (D + UG_BN - 1) / UG_BN;
+  a.Wu_t = Wu_t;
+  a.Wd = Wd;
+  a.y = y;
+  a.ctr = reinterpret_cast<int32_t*>(w + L.ctr);
+  // the gate kernel's block bitmaps when the TwELL has them, else our own
+  const bool own_bits = h->block_bits == nullptr;
+  a.gbm = own_bits ? reinterpret_cast<uint32_t*>(w + L.gbm) : h->block_bits;
+  a.gbm_pitch = own_bits ? static_cast<int32_t>(L.nw) : F / 32;
+  a.nU = reinterpret_cast<int32_t*>(w + L.nU);
+  a.Ulist = reinterpret_cast<int32_t*>(w + L.Ulist);
+  a.units = reinterpret_cast<int32_t*>(w + L.units);
+  a.wpre = reinterpret_cast<int32_t*>(w + L.wpre);
+  a.abuf = reinterpret_cast<uint16_t*>(w + L.abuf);
+  a.status = status_dev;
+
+  // operand maps (box 64 x 128, 128-byte swizzle) and output maps (box
+  // 32 x 32: a in bf16 with the 64-byte swizzle, y in fp32 with 128)
+  CUtensorMap map_x, map_a, map_as, map_y;
+  if ((st = tc_map_a(&map_x, x, T, D, 0)) != TWELL_OK) return st;
+  if ((st = tc_map_a(&map_a, a.abuf, T, L.Fp, 0)) != TWELL_OK) return st;
+  if ((st = make_tmap_2d(&map_as, 2, a.abuf, L.Fp, T, 32, 32, L.Fp * 2, 64)) != TWELL_OK)
+    return st;
+  if ((st = make_tmap_2d(&map_y, 4, y, D, T, 32, 32, static_cast<uint64_t>(D) * 4, 128)) !=
+      TWELL_OK)
+    return st;
+
+  // the counter and our block bitmaps are adjacent: one memset clears both
+  if (cudaMemsetAsync(w + L.ctr, 0, own_bits ? L.nU - L.ctr : 256, s) != cudaSuccess)
+    return TWELL_ERR_CUDA;
+  const dim3 pgrid(a.n_m, UG_BM / UG_ROWS_PER_CTA);
+  if (own_bits) {
+    ug_bits_kernel<<<pgrid, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 4, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  }
+  ug_scan_kernel<<<a.n_m, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 8, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  if ((st = ug_launch<UG_UP>(map_x, map_as, a, a.n_m * a.nj, dev, s)) != TWELL_OK) return st;
+  return ug_launch<UG_DOWN>(map_a, map_y, a, a.n_m * a.nN, dev, s);
+}

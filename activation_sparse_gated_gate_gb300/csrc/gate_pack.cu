@@ -41,6 +41,7 @@ struct GatePackParams {
   int32_t* spill_n;
   int32_t* spill_rt;
   float* spill_val;
+  uint32_t* block_bits;  // optional [num_m][F / 32]
   float* z_debug;
   int32_t* status;
 };
@@ -200,6 +201,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r[ch]);
         ptx::tmem_wait_ld();
+        // bitmask of the positive gates of each 32-column chunk of the row
+        uint32_t mk[4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (__uint_as_float(r[ch][i]) > 0.0f) m |= 1u << i;
+          mk[ch] = valid ? m : 0u;
+        }
+        if (p.block_bits) {
+          // OR over the warp's 32 rows, one atomic per word and warp
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t any = __reduce_or_sync(0xffffffffu, mk[ch]);
+            if (lane == 0 && any)
+              atomicOr(p.block_bits + static_cast<size_t>(m_blk) * (p.F / 32) + kt * 4 + ch, any);
+          }
+        }
         int c = 0;
         if (valid) {
           if (p.z_debug) {
@@ -215,10 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
-            uint32_t m = 0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (__uint_as_float(r[ch][i]) > 0.0f) m |= 1u << i;
+            const uint32_t m = mk[ch];
             if (m == 0u) continue;
             const int n = __popc(m);
             if (c < W) {
@@ -328,10 +345,16 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
   p.spill_n = out->spill_n;
   p.spill_rt = out->spill_rt;
   p.spill_val = out->spill_val;
+  p.block_bits = out->block_bits;
   p.z_debug = z_debug;
   p.status = status_dev;
 
   if (cudaMemsetAsync(out->spill_n, 0, sizeof(int32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
+  if (out->block_bits &&
+      cudaMemsetAsync(out->block_bits, 0,
+                      static_cast<size_t>(p.num_m) * (F / 32) * sizeof(uint32_t), s) !=
+          cudaSuccess)
+    return TWELL_ERR_CUDA;
 
   // Wide tiles (N = 256, two TwELL tiles per accumulator) when they still
   // give every SM work; N = 128 otherwise (few token rows).

@@ -83,9 +83,15 @@ enum {
  *   spill_val[s*tile + c]     fp32 ReLU(z) of column k*tile + c
  *   *spill_n                  slices requested by the last pack (device int32;
  *                             may exceed spill_cap, then TWELL_FLAG_SPILL_FULL)
+ *   block_bits[b*(F/32) + w] optional (may be NULL): bit i of word w is set
+ *                             iff column 32*w + i is active (z > 0) in some row
+ *                             of the block of rows [128 b, 128 b + 128)
+ *                             (every active column counts, spilled or not)
  * Sizes: val [T][n_t][W] float, col [T][n_t][W] uint8, cnt [T][n_t] uint8,
  * spill_slot [T][n_t] int32, spill_rt [spill_cap] int32,
- * spill_val [spill_cap][tile] float.  spill_* may be NULL when spill_cap = 0.
+ * spill_val [spill_cap][tile] float, block_bits [ceil(T/128)][F/32] uint32.
+ * spill_* may be NULL when spill_cap = 0.  A reader trusts block_bits to
+ * describe the same gate as the rest of the TwELL.
  * (The pages leave the value precision open; fp32 keeps the stored gate
  * exact to the accumulator, where bf16 alone would cost up to ~2% of RMS(y).)
  */
@@ -102,6 +108,7 @@ typedef struct {
   int32_t* spill_n;
   int32_t* spill_rt;
   float* spill_val;
+  uint32_t* block_bits;
 } twell_t;
 
 /*
@@ -111,7 +118,8 @@ typedef struct {
  * `*out`.  No dense h is written.
  *   x        [T][D] bf16            Wg_t  [F][D] bf16 (= W_g^T)
  *   out      TwELL with out->T == T, out->F == F; the kernel resets
- *            *out->spill_n to 0 first (stream-ordered)
+ *            *out->spill_n to 0 first (stream-ordered) and, when
+ *            out->block_bits is not NULL, fills it (zeroed first)
  *   z_debug  optional [T][F] fp32 copy of z (NULL to skip), for checking
  *   status_dev  device int32, see TWELL_FLAG_*
  * T may be 0 (nothing enqueued).
@@ -137,6 +145,31 @@ twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T,
 twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
                            const uint16_t* Wd, int32_t D, float* y, int32_t* status_dev,
                            void* stream);
+
+/*
+ * Tensor-core variant of twell_ffn_fwd (paper section 2.B.2: up and down
+ * projections of the active neurons only, built to keep the tensor cores
+ * busy).  Same function, different arithmetic: for each block of 128 rows
+ * the union U of the rows' active neurons (h->block_bits when it is not
+ * NULL, else built from the slots and spill slices) is gathered, u = x W_u[:, U] is
+ * one tcgen05 GEMM, a = h u is rounded to bf16 at each row's own active
+ * neurons (0 at the union's other positions), and y = a W_d[U, :] is a second
+ * tcgen05 GEMM with fp32 accumulation.  The bf16 rounding of h u adds up to
+ * 2^-8 |h u| per term to y (TwELL-exact in everything else, fp32 sums).
+ *   x [T][D] bf16, T = h->T, D a multiple of 64;  Wu_t, Wd [F][D] bf16,
+ *   F = h->F <= 32768;  y [T][D] fp32 (every row written)
+ *   ws: twell_workspace_size(TWELL_WS_FFN_FWD_TC, T, D, F, 0, 0) bytes,
+ *       256-byte aligned (per-block unions and position prefixes, and the
+ *       [T][F] bf16 matrix of a in union order: about 2 T F bytes)
+ * A (row, tile) whose spill slice is missing is skipped and
+ * TWELL_FLAG_SPILL_FULL is set.  Results do not depend on how the work is
+ * scheduled: repeated calls agree bit for bit.  T may be 0.
+ * Returns TWELL_ERR_UNSUPPORTED for F > 32768, TWELL_ERR_INVALID for a D
+ * that is not a multiple of 64 or a workspace that is too small.
+ */
+twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
+                              const uint16_t* Wd, int32_t D, float* y, void* ws,
+                              size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
  * Hybrid training format (paper section 2.B.3): rows whose every tile count
@@ -191,7 +224,8 @@ enum {
   TWELL_WS_HYBRID_FWD = 1,
   TWELL_WS_HYBRID_BWD = 2,
   TWELL_WS_HYBRID_FWD_TC = 3,
-  TWELL_WS_HYBRID_BWD_TC = 4
+  TWELL_WS_HYBRID_BWD_TC = 4,
+  TWELL_WS_FFN_FWD_TC = 5  /* twell_ffn_fwd_tc; cap and max_dense are ignored */
 };
 
 /*

@@ -69,7 +69,7 @@ FAKE = 0x10000  # aligned, never dereferenced: validation fails before any devic
 
 
 def _struct(T=4, F=256, tile=128, width=8, spill_cap=16, ptr=FAKE):
-    return tw.TwellStruct(T, F, tile, width, ptr, ptr, ptr, ptr, spill_cap, ptr, ptr, ptr)
+    return tw.TwellStruct(T, F, tile, width, ptr, ptr, ptr, ptr, spill_cap, ptr, ptr, ptr, None)
 
 
 def _pack(lib, s, T=4, D=64, F=256, x=FAKE, w=FAKE, z=None):

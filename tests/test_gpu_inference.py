@@ -56,6 +56,28 @@ def test_gate_pack_bit_exact(T, D, F, p, W):
     assert int(h.status.item()) == 0
 
 
+def block_bits_reference(zg):
+    """Per block of 128 rows, bit i of word w set iff column 32 w + i has a
+    positive gate in some row of the block (the TwELL block bitmap)."""
+    T, F = zg.shape
+    nb = (T + 127) // 128
+    act = np.zeros((nb * 128, F), dtype=bool)
+    act[:T] = zg > 0
+    anyb = act.reshape(nb, 128, F).any(axis=1).reshape(nb, F // 32, 32)
+    weights = (np.uint64(1) << np.arange(32, dtype=np.uint64))
+    return (anyb.astype(np.uint64) * weights).sum(axis=2).astype(np.uint32)
+
+
+@pytest.mark.parametrize("T,D,F,p,W", SMALL)
+def test_gate_pack_block_bits_bit_exact(T, D, F, p, W):
+    w = workloads.random_small(T, D, F, p, W, seed=T + D)
+    _, h, z = run_pack(w)
+    torch.cuda.synchronize()
+    zg = _check_z(w, z)
+    got = h.block_bits.cpu().numpy().view(np.uint32)
+    np.testing.assert_array_equal(got, block_bits_reference(zg))
+
+
 @pytest.mark.parametrize("T,D,F,p,W", SMALL)
 def test_ffn_fwd_parity(T, D, F, p, W):
     w = workloads.random_small(T, D, F, p, W, seed=T + D)
