@@ -1,8 +1,10 @@
 """Benchmark of the activation-sparse gated FFN (TwELL) inference step on GB300.
 
 One step = one pass of the inference hot path over one batch: the gate GEMM
-with the TwELL-packing epilogue (twell_gate_pack) followed by the fused
-up+down projection (twell_ffn_fwd).  Default workload: the 0.5B-class layer,
+with the TwELL-packing epilogue (twell_gate_pack) followed by the up+down
+projection.  The headline step uses the tensor-core union-gather forward
+(twell_ffn_fwd_tc); the CUDA-core fused kernel (twell_ffn_fwd) is timed in the
+same run and reported beside it.  Default workload: the 0.5B-class layer,
 T=8192 tokens, d_model=1536, d_ff=6144, ~1% active gate neurons, TwELL width
 8 (seeded synthetic inputs, see workloads.py).
 
@@ -258,6 +260,13 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ GPU path
+
+def _block_unions(h, T, F):
+    """Sum over the 128-token blocks of the number of neurons active in some
+    row of the block (the gate kernel's block bitmaps)."""
+    bits = h.block_bits.cpu().numpy().view(np.uint8)
+    return int(np.unpackbits(bits).sum())
+
 
 def fma_peak_tflops(sm_count, sm_mhz):
     """FP32 FMA peak: 128 FP32 lanes per SM (4 sub-partitions x 32), 2 flops
@@ -524,13 +533,20 @@ def run_ours(args, w):
     x, Wg, Wu, Wd = up(w.x), up(w.Wg_t), up(w.Wu_t), up(w.Wd)
     h = tw.TwELL(w.T, w.F, w.width, device=dev)
     y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    y_cc = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    ws_tc = torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC, w.T, w.D, w.F, 0, 0),),
+                        dtype=torch.uint8, device=dev)
     flush = torch.empty((0 if args.no_flush else 512) * 1024 * 1024, dtype=torch.uint8,
                         device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         tw.twell_gate_pack(x, Wg, h, stream=stream)
-        tw.twell_ffn_fwd(x, h, Wu, Wd, y=y, stream=stream)
+        tw.twell_ffn_fwd_tc(x, h, Wu, Wd, y=y, ws=ws_tc, stream=stream)
+
+    def step_cc():
+        tw.twell_gate_pack(x, Wg, h, stream=stream)
+        tw.twell_ffn_fwd(x, h, Wu, Wd, y=y_cc, stream=stream)
 
     # active-neuron union (for the fused kernel's algorithmic bytes), from
     # one untimed pack with the gate pre-activations exported
@@ -541,12 +557,18 @@ def run_ours(args, w):
     for _ in range(args.warmup):
         flush.zero_()
         step()
+        flush.zero_()
+        step_cc()
     torch.cuda.synchronize()
     if int(h.status.item()) != 0:
         raise RuntimeError(f"device status flags {int(h.status.item())}")
 
+    # Each timed iteration runs both steps, each after its own L2 flush: the
+    # headline (gate + tensor-core forward) and the CUDA-core one (gate +
+    # fused kernel); events split every step into its two calls.
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -556,16 +578,31 @@ def run_ours(args, w):
             ev[i][0].record(stream)
             tw.twell_gate_pack(x, Wg, h, stream=stream)
             ev[i][1].record(stream)
-            tw.twell_ffn_fwd(x, h, Wu, Wd, y=y, stream=stream)
+            tw.twell_ffn_fwd_tc(x, h, Wu, Wd, y=y, ws=ws_tc, stream=stream)
             ev[i][2].record(stream)
+            flush.zero_()
+            evc[i][0].record(stream)
+            tw.twell_gate_pack(x, Wg, h, stream=stream)
+            evc[i][1].record(stream)
+            tw.twell_ffn_fwd(x, h, Wu, Wd, y=y_cc, stream=stream)
+            evc[i][2].record(stream)
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     t_k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    t_k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    total_ms = max_over_ranks(sum(a + b for a, b in zip(t_k1, t_k2)), dev)
+    t_tc = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    t_k1c = [evc[i][0].elapsed_time(evc[i][1]) for i in range(K)]
+    t_k2 = [evc[i][1].elapsed_time(evc[i][2]) for i in range(K)]
+    total_ms = max_over_ranks(sum(a + b for a, b in zip(t_k1, t_tc)), dev)
     ms_step = total_ms / K
     value = job_tokens_per_s(w.T, ws, ms_step)
+    cc_ms = max_over_ranks(sum(a + b for a, b in zip(t_k1c, t_k2)), dev) / K
+    if int(h.status.item()) != 0:
+        raise RuntimeError(f"device status flags {int(h.status.item())}")
+    # the two forwards compute the same y up to the bf16 rounding of h u
+    rel = float((y - y_cc).norm() / y_cc.norm())
+    if not rel < 5e-3:
+        raise RuntimeError(f"tensor-core and CUDA-core forwards differ (relative {rel:.2e})")
 
     # end to end through the public API with host buffers: pinned x in, y out.
     # The batch is cut into E_CHUNKS token chunks on three streams (copy in,
@@ -578,6 +615,9 @@ def run_ours(args, w):
     bounds = [w.T * c // E_CHUNKS for c in range(E_CHUNKS + 1)]
     hs = [tw.TwELL(bounds[c + 1] - bounds[c], w.F, w.width, device=dev)
           for c in range(E_CHUNKS)]
+    wss = [torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC, bounds[c + 1] - bounds[c],
+                                                w.D, w.F, 0, 0),), dtype=torch.uint8, device=dev)
+           for c in range(E_CHUNKS)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
     def pipelined_step(origin):
@@ -591,7 +631,7 @@ def run_ours(args, w):
             s_cmp.wait_stream(s_in)
             with torch.cuda.stream(s_cmp):
                 tw.twell_gate_pack(x[a:b], Wg, hs[c], stream=s_cmp)
-                tw.twell_ffn_fwd(x[a:b], hs[c], Wu, Wd, y=y[a:b], stream=s_cmp)
+                tw.twell_ffn_fwd_tc(x[a:b], hs[c], Wu, Wd, y=y[a:b], ws=wss[c], stream=s_cmp)
             s_out.wait_stream(s_cmp)
             with torch.cuda.stream(s_out):
                 yh[a:b].copy_(y[a:b], non_blocking=True)
@@ -626,9 +666,16 @@ def run_ours(args, w):
     hbm, bf16, bf16_sus, src = _peaks()
     k1_ms = statistics.mean(t_k1)
     k2_ms = statistics.mean(t_k2)
+    tc_ms = statistics.mean(t_tc)
     nnz = int(h.cnt.to(torch.int64).sum().item())
     k1_flops = 2.0 * w.T * w.D * w.F
     k1_tf = k1_flops / (k1_ms * 1e-3) / 1e12
+    # tensor-core forward: its two GEMMs over each 128-token block's union of
+    # active neurons, 2 * 128 * D * |U| flops each (the algorithmic work of
+    # the formulation; padding rows and union positions are not counted)
+    blk_union = _block_unions(h, w.T, w.F)
+    tc_flops = 2 * 2.0 * 128 * w.D * blk_union
+    tc_tf = tc_flops / (tc_ms * 1e-3) / 1e12
     # fused kernel: algorithmic bytes = x in (bf16) + y out (fp32) + W_u/W_d
     # rows of every neuron active in some row + the TwELL entries read (5 B
     # per nnz: fp32 value + u8 column, 1 B per count)
@@ -636,31 +683,42 @@ def run_ours(args, w):
     k2_gbs = k2_bytes / (k2_ms * 1e-3) / 1e9
     kernels = {
         "twell_gate_pack": {"ms": k1_ms, "tflops": k1_tf, "frac_bf16": k1_tf / bf16},
+        "twell_ffn_fwd_tc": {"ms": tc_ms, "tflops": tc_tf, "frac_bf16": tc_tf / bf16,
+                             "block_union_mean": blk_union / ((w.T + 127) // 128),
+                             "what": "union scan + up GEMM + down GEMM (one C-ABI call)"},
         "twell_ffn_fwd": {"ms": k2_ms, "gbs": k2_gbs, "frac_hbm": k2_gbs / hbm,
                           "flops": 4.0 * w.D * nnz},
     }
-    if k1_ms >= k2_ms:
+    # The fused CUDA-core kernel's binding roofline is the FP32 FMA pipe (4 D
+    # flops per active entry against 152 SMs x 128 lanes x 2 flops x clock),
+    # not HBM: its algorithmic bytes take a fraction of the time its FMAs
+    # need.  Both fractions are reported.
+    tr2, prof2 = _traffic("twell_ffn_fwd", w.name)
+    k2_tf = kernels["twell_ffn_fwd"]["flops"] / (k2_ms * 1e-3) / 1e12
+    fma = fma_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
+                          clk_sum.get("sm_max_mhz") or 2070.0)
+    kernels["twell_ffn_fwd"]["tflops"] = k2_tf
+    kernels["twell_ffn_fwd"]["frac_fma"] = k2_tf / fma
+    roof_cc = {"kernel": "twell_ffn_fwd", "bound": "alu", "achieved": k2_tf, "peak": fma,
+               "unit": "TFLOP/s", "frac": k2_tf / fma,
+               "peak_source": "FP32 FMA peak derived from SM count, 128 lanes/SM, max SM clock",
+               "traffic": tr2, "traffic_source": prof2, "algorithmic_bytes": k2_bytes,
+               "hbm": {"achieved": k2_gbs, "peak": hbm, "unit": "GB/s", "frac": k2_gbs / hbm,
+                       "peak_source": f"{src} HBM copy"}}
+    # headline step: the larger of its two calls bounds it
+    if k1_ms >= tc_ms:
         tr, prof = _traffic("twell_gate_pack", w.name)
         roof = {"kernel": "twell_gate_pack", "bound": "tensor", "achieved": k1_tf,
                 "peak": bf16, "unit": "TFLOP/s", "frac": k1_tf / bf16,
                 "peak_source": f"{src} bf16 burst", "traffic": tr, "traffic_source": prof}
     else:
-        # The fused kernel's binding roofline is the FP32 FMA pipe (4 D flops
-        # per active entry against 152 SMs x 128 lanes x 2 flops x clock),
-        # not HBM: its algorithmic bytes take a fraction of the time its FMAs
-        # need.  Both fractions are reported.
-        tr, prof = _traffic("twell_ffn_fwd", w.name)
-        k2_tf = kernels["twell_ffn_fwd"]["flops"] / (k2_ms * 1e-3) / 1e12
-        fma = fma_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count,
-                              clk_sum.get("sm_max_mhz") or 2070.0)
-        kernels["twell_ffn_fwd"]["tflops"] = k2_tf
-        kernels["twell_ffn_fwd"]["frac_fma"] = k2_tf / fma
-        roof = {"kernel": "twell_ffn_fwd", "bound": "alu", "achieved": k2_tf, "peak": fma,
-                "unit": "TFLOP/s", "frac": k2_tf / fma,
-                "peak_source": "FP32 FMA peak derived from SM count, 128 lanes/SM, max SM clock",
-                "traffic": tr, "traffic_source": prof, "algorithmic_bytes": k2_bytes,
-                "hbm": {"achieved": k2_gbs, "peak": hbm, "unit": "GB/s", "frac": k2_gbs / hbm,
-                        "peak_source": f"{src} HBM copy"}}
+        tr, prof = _traffic("twell_ffn_fwd_tc", w.name)
+        roof = {"kernel": "twell_ffn_fwd_tc", "bound": "tensor", "achieved": tc_tf,
+                "peak": bf16, "unit": "TFLOP/s", "frac": tc_tf / bf16,
+                "peak_source": f"{src} bf16 burst",
+                "what": ("one call: union scan + up GEMM + down GEMM; flops = the two GEMMs "
+                         "over each 128-token block's union of active neurons"),
+                "traffic": tr, "traffic_source": prof}
     dense_ms = dense_context_forward(x, Wg, Wu, Wd, flush, stream, 3, K)
     energy = None
     if not args.no_energy:
@@ -688,9 +746,14 @@ def run_ours(args, w):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipeline": (f"{E_CHUNKS} token chunks, copy-in / compute / copy-out streams, "
                              "replayed as one CUDA graph")},
-        "gpu_launches": 2 * K,  # kernels in the device-timed region (e2e: 2 per chunk)
+        # our kernels in the timed region per iteration: gate, union scan, up
+        # and down GEMMs (headline) + gate and fused kernel (CUDA-core step)
+        "gpu_launches": 6 * K,
         "roofline": roof,
         "kernels": kernels,
+        "cuda_core": {"ms_per_step": cc_ms, "tokens_per_s": job_tokens_per_s(w.T, ws, cc_ms),
+                      "what": "gate + fused CUDA-core up/down kernel (twell_ffn_fwd)",
+                      "roofline": roof_cc, "relative_difference_to_headline": rel},
         "dense_context": {
             "ms_per_step": dense_ms, "tokens_per_s": job_tokens_per_s(w.T, ws, dense_ms),
             "what": "torch bf16 dense gated FFN (cuBLAS), all neurons, context only"},
