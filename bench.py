@@ -45,7 +45,10 @@ TRAFFIC = {
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         108.68e6, "csrc/ffn_fwd.cu", "67352d39d43dce0a", "profiles/ffn_fwd_0.5B_T8192.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        44.42e6, "csrc/gate_pack.cu", "3b8274881133bd77", "profiles/gate_pack_0.5B_T8192.md"),
+        44.64e6, "csrc/gate_pack.cu", "7161047be7ce0d3d", "profiles/gate_pack_0.5B_T8192.md"),
+    # the call's three kernels (union scan, up and down GEMMs)
+    ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
+        217.7e6, "csrc/ffn_tc.cu", "fca79265ba057332", "profiles/ffn_fwd_tc_0.5B_T8192.md"),
 }
 
 
