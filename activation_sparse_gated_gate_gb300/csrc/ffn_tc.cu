@@ -26,8 +26,9 @@
 // blocks of 64, four shared-memory stages [A 16 KB][B 32 KB]:
 //   warp 0      TMA producer of the A tiles
 //   warp 1      TMEM allocation (two 256-column accumulators) and MMA issue
-//   warps 2-5   epilogue, one TMEM lane quarter each
-//   warps 6-13  B gather: four groups of two warps, group g filling stage g
+//   warps 2-9   epilogue: two sets of four warps, one TMEM lane quarter per
+//               warp; set s writes columns 128 s .. 128 s + 127 of the tile
+//   warps 10-17 B gather: four groups of two warps, group g filling stage g
 //               (32 copies per thread), marking it full once its copies
 //               have landed and it has fenced them to the async proxy
 // Every wait is bounded (about a second); a wait that runs out sets
@@ -49,19 +50,20 @@ constexpr int UG_A = UG_BM * UG_BK * 2;
 constexpr int UG_B = UG_BN * UG_BK * 2;
 constexpr int UG_STAGE = UG_A + UG_B;
 constexpr int UG_GROUP = 64;            // threads of a gather group (one per stage)
-constexpr int UG_GATHER0 = 192;         // first thread of the gather groups
+constexpr int UG_EPI = 256;             // epilogue threads: two sets of four warps
+constexpr int UG_GATHER0 = 64 + UG_EPI; // first thread of the gather groups
 constexpr int UG_THREADS = UG_GATHER0 + UG_ST * UG_GROUP;
-constexpr int UG_HSLOTS = 32;           // up epilogue: gate values staged per row
+constexpr int UG_HSLOTS = 16;           // up epilogue: gate values staged per row and set
 
-// Shared memory: [stages][output staging: 4 warps x 2 buffers of a 32 x 32
-// chunk][barriers 256 B][up: gate-value slots 128 x UG_HSLOTS fp32]
+// Shared memory: [stages][output staging: 8 epilogue warps x one 32 x 32
+// chunk][barriers 256 B][up: gate-value slots 2 sets x 128 rows x UG_HSLOTS fp32]
 template <int MODE>
 struct UgSmem {
   static constexpr int STG_BUF = MODE == 0 ? 32 * 32 * 2 : 32 * 32 * 4;
   static constexpr int STG = UG_ST * UG_STAGE;
   static constexpr int BARS = STG + 8 * STG_BUF;
   static constexpr int SLOTS = BARS + 256;
-  static constexpr int BYTES = SLOTS + (MODE == 0 ? UG_BM * UG_HSLOTS * 4 : 0) + 1024;
+  static constexpr int BYTES = SLOTS + (MODE == 0 ? 2 * UG_BM * UG_HSLOTS * 4 : 0) + 1024;
 };
 constexpr int UG_PREP_THREADS = 256;
 constexpr int UG_ROWS_PER_CTA = 16;     // preparation: rows per CTA
@@ -373,11 +375,14 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
   uint64_t* tfull = empty + UG_ST;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  float* hslots = reinterpret_cast<float*>(smem + SM::SLOTS);  // up: [128][UG_HSLOTS]
+  float* hslots = reinterpret_cast<float*>(smem + SM::SLOTS);  // up: [2][128][UG_HSLOTS]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_units = MODE == UG_UP ? *p.ctr : p.n_m * p.nN;
+  // every role reads the next unit's record one unit ahead
+  UgUnit Un{};
+  if (static_cast<int>(blockIdx.x) < num_units) Un = ug_unit<MODE>(p, blockIdx.x);
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < UG_ST; ++s) {
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 128);
+      ptx::mbar_init(&tempty[a], UG_EPI);
     }
     ptx::fence_mbar_init();
   }
@@ -405,7 +410,9 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const UgUnit U = ug_unit<MODE>(p, u);
+        const UgUnit U = Un;
+        if (u + static_cast<int>(gridDim.x) < num_units)
+          Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
         for (int kb = 0; kb < U.kb; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
             atomicOr(p.status, TWELL_FLAG_TIMEOUT);
@@ -429,7 +436,9 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const UgUnit U = ug_unit<MODE>(p, u);
+        const UgUnit U = Un;
+        if (u + static_cast<int>(gridDim.x) < num_units)
+          Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
         if (U.kb == 0) continue;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
@@ -465,7 +474,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
         ptx::mma_commit(&tfull[acc]);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= UG_GATHER0 / 32) {
     // --------------------------------------------------------- B gather
     // Group grp (64 threads) fills stage grp, i.e. the K blocks whose stage
     // sequence number is grp mod 4: wait for the stage to be free, issue 32
@@ -489,8 +498,11 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
     uint64_t* eb = &empty[grp];
     int seq = 0;
     int ids[32];
+    int ids_for = -1;  // up: the unit whose neuron ids are in ids[]
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const UgUnit U = ug_unit<MODE>(p, u);
+      const UgUnit U = Un;
+      if (u + static_cast<int>(gridDim.x) < num_units)
+        Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
       if (U.kb == 0) continue;
       const int32_t* Ul = p.Ulist + static_cast<size_t>(U.m) * p.Fp;
       // first K block of this unit that is this group's
@@ -501,8 +513,10 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       int col = 0;
       uint32_t nbytes = 16;
       if (MODE == UG_UP) {
+        if (ids_for != u) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ids[i] = __ldg(Ul + U.j * 256 + (g >> 3) + 8 * i);
+          for (int i = 0; i < 32; ++i) ids[i] = __ldg(Ul + U.j * 256 + (g >> 3) + 8 * i);
+        }
       } else {
         col = U.j * UG_BN + 64 * ((g >> 3) & 3) + 8 * cj;
         nbytes = col < p.D ? 16u : 0u;
@@ -537,6 +551,14 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           }
         }
         ptx::cp_async_commit();
+        if (MODE == UG_UP && kb + UG_ST >= U.kb && u + static_cast<int>(gridDim.x) < num_units) {
+          // the copies read their addresses at issue: load the next unit's
+          // ids now, while this stage lands
+          const int32_t* Uln = p.Ulist + static_cast<size_t>(Un.m) * p.Fp;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ids[i] = __ldg(Uln + Un.j * 256 + (g >> 3) + 8 * i);
+          ids_for = u + static_cast<int>(gridDim.x);
+        }
         ptx::cp_async_wait<0>();
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(fb);
@@ -546,15 +568,19 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int set = (warp - 2) >> 2;  // column half of the tile
+    uint8_t* buf = smem + SM::STG + (warp - 2) * SM::STG_BUF;
     int local = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const UgUnit U = ug_unit<MODE>(p, u);
+      const UgUnit U = Un;
+      if (u + static_cast<int>(gridDim.x) < num_units)
+        Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
       const int t = U.m * UG_BM + r;
       const bool valid = t < p.T;
       if (MODE == UG_DOWN && U.kb == 0) {  // no active neuron in the block: y rows are zero
         if (valid) {
-          float* o = p.y + static_cast<size_t>(t) * p.D + U.j * UG_BN;
-          for (int n = 0; n < UG_BN && U.j * UG_BN + n < p.D; n += 4)
+          float* o = p.y + static_cast<size_t>(t) * p.D + U.j * UG_BN + 128 * set;
+          for (int n = 0; n < 128 && U.j * UG_BN + 128 * set + n < p.D; n += 4)
             *reinterpret_cast<float4*>(o + n) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         continue;
@@ -562,43 +588,45 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       ++local;
-      // Up: the row's active positions in the chunk (positions 256 j ..
-      // 256 j + 255 of U, i.e. neurons U[256 j] .. U[last]) as eight mask
-      // words, and the gate values of the first UG_HSLOTS of them (ascending)
-      // in the row's shared-memory slots.  They come from the row's TwELL
-      // tiles that cover those neurons, four tiles' counts and slots loaded
-      // at a time, while the chunk's MMAs run.
-      uint32_t mq[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      float* myslot = hslots + r * UG_HSLOTS;
+      // Up: the row's active positions in this set's half of the chunk
+      // (positions ps .. ps + 127 of U, ps = 256 j + 128 set, i.e. neurons
+      // U[ps] .. U[last]) as four mask words, and the gate values of the
+      // first UG_HSLOTS of them (ascending) in the row's shared-memory slots.
+      // They come from the row's TwELL tiles that cover those neurons, four
+      // tiles' counts and slots loaded at a time, while the chunk's MMAs run.
+      uint32_t mq[4] = {0u, 0u, 0u, 0u};
+      float* myslot = hslots + (set * UG_BM + r) * UG_HSLOTS;
       const int32_t* Ul = p.Ulist + static_cast<size_t>(U.m) * p.Fp;
-      const int p0 = 256 * U.j;
+      const int ps = 256 * U.j + 128 * set;
       if (MODE == UG_UP && valid) {
         const int nUm = __ldg(p.nU + U.m);
-        const int lo_n = __ldg(Ul + p0);
-        const int hi_n = __ldg(Ul + min(p0 + 255, nUm - 1));
-        const uint32_t* bmr = p.gbm + static_cast<size_t>(U.m) * p.gbm_pitch;
-        const int32_t* wpr = p.wpre + static_cast<size_t>(U.m) * p.nw;
-        int nset = 0;
-        auto add = [&](int n, float h) {
-          if (n < lo_n || n > hi_n) return;
-          const int w = n >> 5;
-          const int pos =
-              __ldg(wpr + w) + __popc(__ldg(bmr + w) & ((1u << (n & 31)) - 1u)) - p0;
-          const uint32_t bit = 1u << (pos & 31);
-          const uint32_t wsel = pos >> 5;  // a select per word, not an index
+        if (ps < nUm) {
+          const int lo_n = __ldg(Ul + ps);
+          const int hi_n = __ldg(Ul + min(ps + 127, nUm - 1));
+          const uint32_t* bmr = p.gbm + static_cast<size_t>(U.m) * p.gbm_pitch;
+          const int32_t* wpr = p.wpre + static_cast<size_t>(U.m) * p.nw;
+          int nset = 0;
+          auto add = [&](int n, float h) {
+            if (n < lo_n || n > hi_n) return;
+            const int w = n >> 5;
+            const int pos =
+                __ldg(wpr + w) + __popc(__ldg(bmr + w) & ((1u << (n & 31)) - 1u)) - ps;
+            const uint32_t bit = 1u << (pos & 31);
+            const uint32_t wsel = pos >> 5;  // a select per word, not an index
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mq[k] |= (wsel == static_cast<uint32_t>(k) ? bit : 0u);
-          if (nset < UG_HSLOTS) myslot[nset] = h;
-          ++nset;
-        };
-        const size_t rtb = static_cast<size_t>(t) * p.n_t;
-        const int k0 = lo_n >> 7, k1 = hi_n >> 7;
-        if (p.W == 8) {
-          walk_tiles<8, 4>(p, rtb, k0, k1, add);
-        } else if (p.W == 16) {
-          walk_tiles<16, 2>(p, rtb, k0, k1, add);
-        } else {
-          for (int k = k0; k <= k1; ++k) ug_walk_pair(p, rtb + k, k, false, add);
+            for (int k = 0; k < 4; ++k) mq[k] |= (wsel == static_cast<uint32_t>(k) ? bit : 0u);
+            if (nset < UG_HSLOTS) myslot[nset] = h;
+            ++nset;
+          };
+          const size_t rtb = static_cast<size_t>(t) * p.n_t;
+          const int k0 = lo_n >> 7, k1 = hi_n >> 7;
+          if (p.W == 8) {
+            walk_tiles<8, 4>(p, rtb, k0, k1, add);
+          } else if (p.W == 16) {
+            walk_tiles<16, 2>(p, rtb, k0, k1, add);
+          } else {
+            for (int k = k0; k <= k1; ++k) ug_walk_pair(p, rtb + k, k, false, add);
+          }
         }
       }
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
@@ -606,34 +634,40 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
         goto done;
       }
       ptx::tc_fence_after();
-      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * UG_BN) +
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * UG_BN + 128 * set) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      // Output chunks of 32 columns go through a per-warp staging buffer
-      // (two per warp, alternating): each lane writes its row with the
-      // swizzle of the output tensor map (16-byte chunk j of row r at chunk
-      // j ^ (address bits 7..)), conflict-free, and lane 0 stores the warp's
-      // 32 x 32 box with one TMA store (rows past T are clipped).
+      // Output chunks of 32 columns go through the warp's staging buffer:
+      // each lane writes its row with the swizzle of the output tensor map
+      // (16-byte chunk j of row r at chunk j ^ (address bits 7..)),
+      // conflict-free, and lane 0 stores the warp's 32 x 32 box with one TMA
+      // store (rows past T are clipped); the buffer is reused once that
+      // store has read it.
       const int row0 = U.m * UG_BM + q * 32;
-      if (MODE == UG_UP) {
-        int rank = 0;  // active positions of the row consumed so far
+      // chunks of this set (down: the tile may end before the second half)
+      const int nch = MODE == UG_UP ? 4 : max(0, min(128, p.D - U.j * UG_BN - 128 * set) / 32);
+      if (nch == 0) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tempty[acc]);
+      }
+      int rank = 0;  // up: active positions of the row consumed so far
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
-          ptx::tmem_wait_ld();
-          if (c == 7) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&tempty[acc]);
-          }
+      for (int c = 0; c < nch; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+        ptx::tmem_wait_ld();
+        if (c == nch - 1) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&tempty[acc]);
+        }
+        if (lane == 0) ptx::bulk_wait_read<0>();
+        __syncwarp();
+        if (MODE == UG_UP) {
           uint32_t mc = mq[0];
 #pragma unroll
-          for (int i = 0; i < 7; ++i) mq[i] = mq[i + 1];
+          for (int i = 0; i < 3; ++i) mq[i] = mq[i + 1];
           // 64-byte rows, 64-byte swizzle: chunk j of row lane at j ^ ((lane >> 1) & 3).
           // The row is zeroed, then each active position gets its bf16 a;
           // the loop runs as often as the busiest lane of the warp needs.
-          uint8_t* buf = smem + SM::STG + (q * 2 + (c & 1)) * SM::STG_BUF;
-          if (lane == 0) ptx::bulk_wait_read<1>();
-          __syncwarp();
           uint8_t* my_row = buf + lane * 64;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -645,45 +679,26 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
               mc &= mc - 1u;
               const float hv = rank < UG_HSLOTS
                                    ? myslot[rank]
-                                   : twell_h_at(p, t, __ldg(Ul + p0 + 32 * c + i));
+                                   : twell_h_at(p, t, __ldg(Ul + ps + 32 * c + i));
               ++rank;
               const float a = hv * __uint_as_float(select32(v, i));
               *reinterpret_cast<uint16_t*>(my_row + ((((i >> 3) ^ sw)) << 4) + (i & 7) * 2) =
                   __bfloat16_as_ushort(__float2bfloat16_rn(a));
             }
           }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(&map_out, buf, 256 * U.j + 32 * c, row0);
-            ptx::bulk_commit();
-          }
-        }
-      } else {
-        const int nch = min(UG_BN, p.D - U.j * UG_BN) / 32;
-#pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
-          ptx::tmem_wait_ld();
-          if (c == nch - 1) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&tempty[acc]);
-          }
+        } else {
           // 128-byte rows, 128-byte swizzle: chunk j of row lane at j ^ (lane & 7)
-          uint8_t* buf = smem + SM::STG + (q * 2 + (c & 1)) * SM::STG_BUF;
-          if (lane == 0) ptx::bulk_wait_read<1>();
-          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                 make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(&map_out, buf, U.j * UG_BN + 32 * c, row0);
-            ptx::bulk_commit();
-          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&map_out, buf, (MODE == UG_UP ? 256 : UG_BN) * U.j + 128 * set + 32 * c,
+                            row0);
+          ptx::bulk_commit();
         }
       }
     }
@@ -691,7 +706,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
 
 done:
   // the epilogue's TMA stores have finished before the CTA's shared memory goes away
-  if (warp >= 2 && warp < 6 && lane == 0) ptx::bulk_wait_all();
+  if (warp >= 2 && warp < UG_GATHER0 / 32 && lane == 0) ptx::bulk_wait_all();
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
