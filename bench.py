@@ -48,7 +48,7 @@ TRAFFIC = {
         44.64e6, "csrc/gate_pack.cu", "7161047be7ce0d3d", "profiles/gate_pack_0.5B_T8192.md"),
     # the call's three kernels (union scan, up and down GEMMs)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        217.7e6, "csrc/ffn_tc.cu", "fca79265ba057332", "profiles/ffn_fwd_tc_0.5B_T8192.md"),
+        219.3e6, "csrc/ffn_tc.cu", "d23884105e7ba2a4", "profiles/ffn_fwd_tc_0.5B_T8192.md"),
 }
 
 
@@ -627,6 +627,27 @@ def run_ours(args, w):
            for c in range(E_CHUNKS)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
+    # the chunks are E_CHUNKS times smaller than the batch: time both
+    # forwards once at the chunk size and pipeline the faster
+    def _chunk_ms(fwd_tc):
+        c_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for it in range(4):
+            if it == 1:
+                c_ev[0].record(stream)
+            for c in range(E_CHUNKS):
+                a, b = bounds[c], bounds[c + 1]
+                tw.twell_gate_pack(x[a:b], Wg, hs[c], stream=stream)
+                if fwd_tc:
+                    tw.twell_ffn_fwd_tc(x[a:b], hs[c], Wu, Wd, y=y[a:b], ws=wss[c],
+                                        stream=stream)
+                else:
+                    tw.twell_ffn_fwd(x[a:b], hs[c], Wu, Wd, y=y[a:b], stream=stream)
+        c_ev[1].record(stream)
+        torch.cuda.synchronize()
+        return c_ev[0].elapsed_time(c_ev[1])
+
+    chunk_tc = _chunk_ms(True) <= _chunk_ms(False)
+
     def pipelined_step(origin):
         # fork from `origin`, one chunk per stage on each stream, join back
         for st in (s_in, s_cmp, s_out):
@@ -638,7 +659,7 @@ def run_ours(args, w):
             s_cmp.wait_stream(s_in)
             with torch.cuda.stream(s_cmp):
                 tw.twell_gate_pack(x[a:b], Wg, hs[c], stream=s_cmp)
-                if use_tc:
+                if chunk_tc:
                     tw.twell_ffn_fwd_tc(x[a:b], hs[c], Wu, Wd, y=y[a:b], ws=wss[c], stream=s_cmp)
                 else:
                     tw.twell_ffn_fwd(x[a:b], hs[c], Wu, Wd, y=y[a:b], stream=s_cmp)
@@ -757,7 +778,9 @@ def run_ours(args, w):
         "e2e": {"value": job_tokens_per_s(w.T, ws, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipeline": (f"{E_CHUNKS} token chunks, copy-in / compute / copy-out streams, "
-                             "replayed as one CUDA graph")},
+                             "replayed as one CUDA graph"),
+                "forward": ("tensor-core union gather" if chunk_tc
+                            else "CUDA-core fused kernel") + " (the faster at the chunk size)"},
         # our kernels in the timed region per iteration: gate, union scan, up
         # and down GEMMs (headline) + gate and fused kernel (CUDA-core step)
         "gpu_launches": 6 * K,
