@@ -18,11 +18,11 @@ import torch
 
 __all__ = [
     "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
-    "twell_ffn_fwd_tc",
+    "twell_ffn_fwd_tc", "twell_to_f16",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd",
     "twell_status_string",
-    "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "TILE",
+    "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "TILE",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +31,7 @@ TILE = 128
 FLAG_SPILL_FULL = 1
 FLAG_DENSE_FULL = 2
 FLAG_TIMEOUT = 4
+FLAG_RANGE = 8
 
 c_i32 = ctypes.c_int32
 c_ptr = ctypes.c_void_p
@@ -70,8 +71,9 @@ _SIGNATURES = {
                                 c_ptr, c_ptr, c_ptr]),
     "twell_ffn_fwd": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
                               c_ptr, c_ptr]),
-    "twell_ffn_fwd_tc": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
-                                 c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "twell_ffn_fwd_tc": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_ptr, c_i32,
+                                 c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "twell_to_f16": (c_i32, [c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "twell_to_hybrid": (c_i32, [ctypes.POINTER(TwellStruct), ctypes.POINTER(HybridStruct),
                                 c_ptr, c_ptr]),
     "twell_workspace_size": (ctypes.c_size_t, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
@@ -213,11 +215,28 @@ def twell_ffn_fwd(x, h: TwELL, Wu_t, Wd, y=None, status=None, stream=None):
     return y
 
 
-def twell_ffn_fwd_tc(x, h: TwELL, Wu_t, Wd, y=None, ws=None, status=None, stream=None):
+def twell_to_f16(src, dst=None, status=None, stream=None):
+    """fp16 copy of a bf16 tensor (e.g. W_d for ``twell_ffn_fwd_tc``)."""
+    _need(src, torch.bfloat16, "src")
+    if dst is None:
+        dst = torch.empty(src.shape, dtype=torch.float16, device=src.device)
+    if dst.dtype != torch.float16 or not dst.is_contiguous() or dst.shape != src.shape:
+        raise ValueError("dst must be a contiguous fp16 tensor shaped like src")
+    if status is None:
+        status = torch.zeros((1,), dtype=torch.int32, device=src.device)
+    with torch.cuda.device(src.device):
+        _check(lib().twell_to_f16(_ptr(src), _ptr(dst), src.numel(), _ptr(status),
+                                  _stream(stream)), "twell_to_f16")
+    return dst
+
+
+def twell_ffn_fwd_tc(x, h: TwELL, Wu_t, Wd, y=None, ws=None, Wd_f16=None, status=None,
+                     stream=None):
     """Tensor-core (union-gather) up + down projection from the TwELL gate
-    ``h``: the same function as ``twell_ffn_fwd`` with h*u rounded to bf16;
+    ``h``: the same function as ``twell_ffn_fwd`` with h*u rounded to fp16;
     returns y [T][D] fp32 (allocated if not given).  ``ws`` is the device
-    workspace (allocated if not given)."""
+    workspace (allocated if not given); ``Wd_f16`` an optional fp16 copy of
+    ``Wd`` (``twell_to_f16``), made by the call when not given."""
     _need(x, torch.bfloat16, "x")
     _need(Wu_t, torch.bfloat16, "Wu_t")
     _need(Wd, torch.bfloat16, "Wd")
@@ -227,14 +246,18 @@ def twell_ffn_fwd_tc(x, h: TwELL, Wu_t, Wd, y=None, ws=None, status=None, stream
     _need(y, torch.float32, "y")
     if Wu_t.shape != (h.F, D) or Wd.shape != (h.F, D) or T != h.T:
         raise ValueError("shape mismatch: x [T][D], Wu_t and Wd [F][D]")
+    if Wd_f16 is not None and (Wd_f16.dtype != torch.float16 or Wd_f16.shape != Wd.shape
+                               or not Wd_f16.is_contiguous()):
+        raise ValueError("Wd_f16 must be a contiguous fp16 copy of Wd")
     nbytes = twell_workspace_size(WS_FFN_FWD_TC, T, D, h.F, 0, 0)
     if ws is None:
         ws = _workspace(nbytes, x.device)
     status = h.status if status is None else status
     with torch.cuda.device(x.device):
-        _check(lib().twell_ffn_fwd_tc(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd), D,
-                                      _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
-                                      _ptr(status), _stream(stream)),
+        _check(lib().twell_ffn_fwd_tc(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd),
+                                      _ptr(Wd_f16), D, _ptr(y), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(status),
+                                      _stream(stream)),
                "twell_ffn_fwd_tc")
     return y
 

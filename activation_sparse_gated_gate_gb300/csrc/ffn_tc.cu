@@ -7,11 +7,14 @@
 // The rows of a block of 128 tokens share one gathered operand: the union U
 // of their active neurons (ascending).  The forward is then two dense
 // tcgen05 GEMMs over that union alone:
-//   up    u = x_blk . W_u[:, U]          (128 x |U|, K = D), and in the
-//         epilogue a = bf16(h u) at each row's own active neurons, 0 at the
-//         other union positions, written to a [T][Fp] bf16 scratch matrix in
+//   up    u = x_blk . W_u[:, U]          (128 x |U|, K = D, bf16), and in the
+//         epilogue a = fp16(h u) at each row's own active neurons, 0 at the
+//         other union positions, written to a [T][Fp] fp16 scratch matrix in
 //         union-position order
-//   down  y_blk = a_blk . W_d[U, :]      (128 x D, K = |U|), fp32 out
+//   down  y_blk = a_blk . W_d[U, :]      (128 x D, K = |U|, fp16 operands:
+//         W_d converted into the workspace), fp32 out
+// (fp16 for the down GEMM: a bf16 a = h u adds up to 2^-8 |h u| per term,
+// which over 30-40 terms of a row exceeded 2e-2 * RMS(y); fp16 adds 2^-11.)
 // The union's weight rows are gathered into the 128-byte-swizzled operand
 // tiles by four warps with 16-byte cp.async copies (each copy lands where a
 // TMA box with that swizzle would put it); the token tiles (x, a) come by
@@ -34,6 +37,7 @@
 // Every wait is bounded (about a second); a wait that runs out sets
 // TWELL_FLAG_TIMEOUT and the CTA leaves its loops, frees its TMEM and exits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fused.cuh"
 #include "ptx.cuh"
@@ -81,7 +85,8 @@ struct UgArgs {
   int32_t spill_cap;
   int32_t T, D, F, Fp, nw, n_t, W, n_m, nj, nN;
   const uint16_t* Wu_t;
-  const uint16_t* Wd;
+  const uint16_t* Wd;   // bf16 (converted by ug_f16_kernel)
+  uint16_t* Wd16;       // fp16 copy in the workspace (the down GEMM's B)
   float* y;
   // workspace
   int32_t* ctr;     // [0]: units of the up GEMM
@@ -91,18 +96,18 @@ struct UgArgs {
   int32_t* Ulist;   // [n_m][Fp] union neurons, ascending, padded with 0
   int32_t* units;   // [n_m * nj] up-GEMM units (block * nj + chunk)
   int32_t* wpre;    // [n_m][nw] union position of each bitmap word's first bit
-  uint16_t* abuf;   // [T][Fp] a = bf16(h u) in union-position order
+  uint16_t* abuf;   // [T][Fp] a = fp16(h u) in union-position order
   int32_t* status;
 };
 
 struct UgLayout {
-  size_t ctr, gbm, nU, Ulist, units, wpre, abuf, bytes;
+  size_t ctr, gbm, nU, Ulist, units, wpre, abuf, wd16, bytes;
   int64_t Fp, nw, n_m, nj;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-UgLayout ug_layout(int64_t T, int64_t F) {
+UgLayout ug_layout(int64_t T, int64_t D, int64_t F) {
   UgLayout L{};
   L.Fp = (F + 255) / 256 * 256;
   L.nw = L.Fp / 32;
@@ -123,6 +128,8 @@ UgLayout ug_layout(int64_t T, int64_t F) {
   o = up256(o + static_cast<size_t>(L.n_m) * L.nw * 4);
   L.abuf = o;
   o = up256(o + static_cast<size_t>(T) * L.Fp * 2);
+  L.wd16 = o;
+  o = up256(o + static_cast<size_t>(F) * D * 2);
   L.bytes = o;
   return L;
 }
@@ -255,9 +262,35 @@ __global__ void __launch_bounds__(UG_PREP_THREADS) ug_scan_kernel(const UgArgs p
   for (int jn = tid; jn < chunks; jn += UG_PREP_THREADS) p.units[s_base + jn] = m * p.nj + jn;
 }
 
+// bf16 -> fp16 copy of W_d for the down GEMM (8 values per thread and step;
+// exact for |w| in fp16's normal range, |w| >= 2^-14; a |w| above 65504
+// becomes inf and sets TWELL_FLAG_RANGE).
+__global__ void __launch_bounds__(256) ug_f16_kernel(const uint16_t* __restrict__ src,
+                                                     uint16_t* __restrict__ dst, size_t n8,
+                                                     int32_t* status) {
+  bool over = false;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16);
+      const float hi = __uint_as_float(w[k] & 0xffff0000u);
+      over |= fabsf(lo) > 65504.0f || fabsf(hi) > 65504.0f;
+      o[k] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+    }
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (over) atomicOr(status, TWELL_FLAG_RANGE);
+}
+
 // --------------------------------------------------------------- the GEMMs
 struct UgUnit {
   int m, j, kb;  // token block, output chunk (up: union chunk; down: D tile), K blocks
+  int n0;        // first output column (down) or union position (up) of the tile
 };
 
 template <int MODE>
@@ -273,6 +306,7 @@ __device__ __forceinline__ UgUnit ug_unit(const UgArgs& p, int u) {
     r.j = u - r.m * p.nN;
     r.kb = (p.nU[r.m] + UG_BK - 1) / UG_BK;
   }
+  r.n0 = UG_BN * r.j;
   return r;
 }
 
@@ -431,7 +465,9 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(UG_BM, UG_BN, false, MODE == UG_DOWN);
+      // up: bf16 x and W_u; down: fp16 a and W_d
+      constexpr uint32_t idesc = MODE == UG_UP ? ptx::idesc_bf16_f32(UG_BM, UG_BN, false, false)
+                                               : ptx::idesc_f16_f32(UG_BM, UG_BN, false, true);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -518,7 +554,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           for (int i = 0; i < 32; ++i) ids[i] = __ldg(Ul + U.j * 256 + (g >> 3) + 8 * i);
         }
       } else {
-        col = U.j * UG_BN + 64 * ((g >> 3) & 3) + 8 * cj;
+        col = U.n0 + 64 * ((g >> 3) & 3) + 8 * cj;
         nbytes = col < p.D ? 16u : 0u;
         if (col >= p.D) col = 0;
 #pragma unroll
@@ -542,7 +578,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             const int k = (g >> 5) + 2 * i;
             ptx::cp_async16(box + k * 128 + ((cj ^ (k & 7)) << 4),
-                            p.Wd + static_cast<size_t>(ids[i]) * p.D + col, nbytes);
+                            p.Wd16 + static_cast<size_t>(ids[i]) * p.D + col, nbytes);
           }
           if (kb + UG_ST < U.kb) {
 #pragma unroll
@@ -579,8 +615,8 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       const bool valid = t < p.T;
       if (MODE == UG_DOWN && U.kb == 0) {  // no active neuron in the block: y rows are zero
         if (valid) {
-          float* o = p.y + static_cast<size_t>(t) * p.D + U.j * UG_BN + 128 * set;
-          for (int n = 0; n < 128 && U.j * UG_BN + 128 * set + n < p.D; n += 4)
+          float* o = p.y + static_cast<size_t>(t) * p.D + U.n0 + 128 * set;
+          for (int n = 0; n < 128 && U.n0 + 128 * set + n < p.D; n += 4)
             *reinterpret_cast<float4*>(o + n) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         continue;
@@ -644,7 +680,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       // store has read it.
       const int row0 = U.m * UG_BM + q * 32;
       // chunks of this set (down: the tile may end before the second half)
-      const int nch = MODE == UG_UP ? 4 : max(0, min(128, p.D - U.j * UG_BN - 128 * set) / 32);
+      const int nch = MODE == UG_UP ? 4 : max(0, min(128, p.D - U.n0 - 128 * set) / 32);
       if (nch == 0) {
         ptx::tc_fence_before();
         ptx::mbar_arrive(&tempty[acc]);
@@ -682,8 +718,9 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
                                    : twell_h_at(p, t, __ldg(Ul + ps + 32 * c + i));
               ++rank;
               const float a = hv * __uint_as_float(select32(v, i));
+              if (fabsf(a) > 65504.0f) atomicOr(p.status, TWELL_FLAG_RANGE);
               *reinterpret_cast<uint16_t*>(my_row + ((((i >> 3) ^ sw)) << 4) + (i & 7) * 2) =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(a));
+                  __half_as_ushort(__float2half_rn(a));
             }
           }
         } else {
@@ -696,8 +733,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::tma_store_2d(&map_out, buf, (MODE == UG_UP ? 256 : UG_BN) * U.j + 128 * set + 32 * c,
-                            row0);
+          ptx::tma_store_2d(&map_out, buf, U.n0 + 128 * set + 32 * c, row0);
           ptx::bulk_commit();
         }
       }
@@ -733,14 +769,33 @@ twell_status ug_launch(const CUtensorMap& map, const CUtensorMap& map_out, const
 
 }  // namespace
 
-size_t ffn_tc_workspace_bytes(int64_t T, int64_t F) { return ug_layout(T, F).bytes; }
+size_t ffn_tc_workspace_bytes(int64_t T, int64_t D, int64_t F) {
+  return ug_layout(T, D, F).bytes;
+}
 
 }  // namespace twell
 
+extern "C" twell_status twell_to_f16(const uint16_t* src, uint16_t* dst, size_t n,
+                                     int32_t* status_dev, void* stream) {
+  using namespace twell;
+  if (n == 0) return TWELL_OK;
+  if (!src || !dst || !status_dev || n % 8 != 0 || !aligned16(src) || !aligned16(dst))
+    return TWELL_ERR_INVALID;
+  DeviceInfo dev;
+  twell_status st;
+  if ((st = require_sm103(&dev)) != TWELL_OK) return st;
+  const size_t n8 = n / 8;
+  const size_t want = (n8 + 255) / 256;
+  const size_t cap = 4u * static_cast<size_t>(dev.sm_count);
+  ug_f16_kernel<<<static_cast<int>(want < cap ? want : cap), 256, 0,
+                  static_cast<cudaStream_t>(stream)>>>(src, dst, n8, status_dev);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
 extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
-                                         const uint16_t* Wu_t, const uint16_t* Wd, int32_t D,
-                                         float* y, void* ws, size_t ws_bytes,
-                                         int32_t* status_dev, void* stream) {
+                                         const uint16_t* Wu_t, const uint16_t* Wd,
+                                         const uint16_t* Wd_f16, int32_t D, float* y, void* ws,
+                                         size_t ws_bytes, int32_t* status_dev, void* stream) {
   using namespace twell;
   if (h == nullptr) return TWELL_ERR_INVALID;
   const int32_t T = h->T, F = h->F;
@@ -752,9 +807,9 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   if (T == 0) return TWELL_OK;
   if (!x || !Wu_t || !Wd || !y || !status_dev || !ws) return TWELL_ERR_INVALID;
   if (!aligned16(x) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y) ||
-      (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+      (Wd_f16 && !aligned16(Wd_f16)) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return TWELL_ERR_INVALID;
-  const UgLayout L = ug_layout(T, F);
+  const UgLayout L = ug_layout(T, D, F);
   if (ws_bytes < L.bytes) return TWELL_ERR_INVALID;
   DeviceInfo dev;
   if ((st = require_sm103(&dev)) != TWELL_OK) return st;
@@ -791,6 +846,8 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   a.units = reinterpret_cast<int32_t*>(w + L.units);
   a.wpre = reinterpret_cast<int32_t*>(w + L.wpre);
   a.abuf = reinterpret_cast<uint16_t*>(w + L.abuf);
+  // the caller's fp16 copy of W_d, or one made in the workspace below
+  a.Wd16 = Wd_f16 ? const_cast<uint16_t*>(Wd_f16) : reinterpret_cast<uint16_t*>(w + L.wd16);
   a.status = status_dev;
 
   // operand maps (box 64 x 128, 128-byte swizzle) and output maps (box
@@ -814,6 +871,14 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   }
   ug_scan_kernel<<<a.n_m, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 8, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  if (!Wd_f16) {
+    const size_t n8 = static_cast<size_t>(F) * D / 8;  // D % 64 == 0
+    const size_t want = (n8 + 255) / 256;
+    const size_t cap = 4u * static_cast<size_t>(dev.sm_count);
+    ug_f16_kernel<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(Wd, a.Wd16, n8,
+                                                                           status_dev);
+    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  }
   if ((st = ug_launch<UG_UP>(map_x, map_as, a, a.n_m * a.nj, dev, s)) != TWELL_OK) return st;
   return ug_launch<UG_DOWN>(map_a, map_y, a, a.n_m * a.nN, dev, s);
 }

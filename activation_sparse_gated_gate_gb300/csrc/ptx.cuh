@@ -214,6 +214,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = 
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// Same with fp16 A and B (format code 0 in the A and B format fields).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn = false,
+                                                     bool b_mn = false) {
+  return idesc_bf16_f32(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10));
+}
+
 // Named barrier `id` over `count` threads (a multiple of 32).
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

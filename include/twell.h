@@ -62,7 +62,8 @@ typedef enum {
 enum {
   TWELL_FLAG_SPILL_FULL = 1,  /* more (row, tile) slices overflowed W than spill_cap */
   TWELL_FLAG_DENSE_FULL = 2,  /* more overflow rows than the hybrid's max_dense */
-  TWELL_FLAG_TIMEOUT = 4      /* a pipeline wait exceeded its bound (about 1 s) */
+  TWELL_FLAG_TIMEOUT = 4,     /* a pipeline wait exceeded its bound (about 1 s) */
+  TWELL_FLAG_RANGE = 8        /* a value exceeded the fp16 range of an fp16 operand */
 };
 
 #define TWELL_TILE 128
@@ -152,15 +153,22 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
  * busy).  Same function, different arithmetic: for each block of 128 rows
  * the union U of the rows' active neurons (h->block_bits when it is not
  * NULL, else built from the slots and spill slices) is gathered, u = x W_u[:, U] is
- * one tcgen05 GEMM, a = h u is rounded to bf16 at each row's own active
- * neurons (0 at the union's other positions), and y = a W_d[U, :] is a second
- * tcgen05 GEMM with fp32 accumulation.  The bf16 rounding of h u adds up to
- * 2^-8 |h u| per term to y (TwELL-exact in everything else, fp32 sums).
+ * one tcgen05 GEMM (bf16 in, fp32 out), a = h u is rounded to fp16 at each
+ * row's own active neurons (0 at the union's other positions), and
+ * y = a W_d[U, :] is a second tcgen05 GEMM on fp16 operands (W_d converted
+ * from bf16 into the workspace, exactly for |w| >= 2^-14) with fp32
+ * accumulation.  The fp16 rounding of h u adds up to 2^-11 |h u| (+ 2^-25)
+ * per term to y; fp16 rather than bf16 keeps y within the 2e-2 * RMS bar
+ * where a bf16 a (2^-8) did not (30-40 active terms of one row).  A |h u|
+ * beyond the fp16 range (65504) sets TWELL_FLAG_RANGE.
  *   x [T][D] bf16, T = h->T, D a multiple of 64;  Wu_t, Wd [F][D] bf16,
  *   F = h->F <= 32768;  y [T][D] fp32 (every row written)
+ *   Wd_f16  optional [F][D] fp16 copy of Wd (twell_to_f16); NULL: the call
+ *           makes one in the workspace (one extra pass over W_d)
  *   ws: twell_workspace_size(TWELL_WS_FFN_FWD_TC, T, D, F, 0, 0) bytes,
- *       256-byte aligned (per-block unions and position prefixes, and the
- *       [T][F] bf16 matrix of a in union order: about 2 T F bytes)
+ *       256-byte aligned (per-block unions and position prefixes, the
+ *       [T][F] fp16 matrix of a in union order and the fp16 copy of W_d:
+ *       about 2 (T + D) F bytes)
  * A (row, tile) whose spill slice is missing is skipped and
  * TWELL_FLAG_SPILL_FULL is set.  Results do not depend on how the work is
  * scheduled: repeated calls agree bit for bit.  T may be 0.
@@ -168,8 +176,18 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
  * that is not a multiple of 64 or a workspace that is too small.
  */
 twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
-                              const uint16_t* Wd, int32_t D, float* y, void* ws,
-                              size_t ws_bytes, int32_t* status_dev, void* stream);
+                              const uint16_t* Wd, const uint16_t* Wd_f16, int32_t D, float* y,
+                              void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * fp16 copy of bf16 values (for the W_d operand of twell_ffn_fwd_tc, made
+ * once for weights that do not change between calls): dst[i] = fp16(src[i]),
+ * round to nearest; exact for |v| >= 2^-14 (bf16 has fewer significant
+ * bits); |v| > 65504 becomes inf and sets TWELL_FLAG_RANGE.
+ *   src, dst  device arrays of n elements, 16-byte aligned, n a multiple of 8
+ */
+twell_status twell_to_f16(const uint16_t* src, uint16_t* dst, size_t n, int32_t* status_dev,
+                          void* stream);
 
 /*
  * Hybrid training format (paper section 2.B.3): rows whose every tile count
