@@ -13,9 +13,11 @@
 // the row count may be a device value (number of overflow rows), in which
 // case row tiles past it are skipped by every role.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gemm.cuh"
 #include "ptx.cuh"
+#include "scale.cuh"
 
 namespace twell {
 namespace {
@@ -456,14 +458,14 @@ template <int MODE>
 __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
   const int R_act = a.R_dyn ? min(a.R, *a.R_dyn) : a.R;
   const int R_out = a.pad > 0 ? min(a.R, (R_act + a.pad - 1) / a.pad * a.pad) : R_act;
-  const int per_row = MODE == 1 ? a.C / 4 : a.C / 8;
+  const int per_row = (MODE == 1 || MODE == 3) ? a.C / 4 : a.C / 8;
   const long long total = static_cast<long long>(R_out) * per_row;
   for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
        v += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int i = static_cast<int>(v / per_row);
     const int q = static_cast<int>(v % per_row);
     if (i >= R_act) {  // zero padding rows
-      if (MODE == 1) {
+      if (MODE == 1 || MODE == 3) {
         uint16_t* o = a.out + static_cast<int64_t>(i) * a.ldo + 4 * q;
         reinterpret_cast<uint2*>(o)[0] = make_uint2(0u, 0u);
         reinterpret_cast<uint2*>(o + a.C)[0] = make_uint2(0u, 0u);
@@ -474,7 +476,48 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
       continue;
     }
     const int64_t sr = a.row_idx ? a.row_idx[i] : i;
-    if (MODE == 2) {
+    if (MODE == 3) {
+      const float4 x =
+          reinterpret_cast<const float4*>(static_cast<const float*>(a.src) + sr * a.lds)[q];
+      const float sc = a.amax ? pow2_scale(a.amax, a.amax_floor, false) : 1.0f;
+      const float f[4] = {sc * x.x, sc * x.y, sc * x.z, sc * x.w};
+      uint32_t h[4], l[4];
+      bool over = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        over |= fabsf(f[e]) > 65504.0f;
+        const __half hv = __float2half_rn(f[e]);
+        h[e] = __half_as_ushort(hv);
+        l[e] = __half_as_ushort(__float2half_rn(f[e] - __half2float(hv)));
+      }
+      if (over && a.status) atomicOr(a.status, TWELL_FLAG_RANGE);
+      uint16_t* o = a.out + static_cast<int64_t>(i) * a.ldo + 4 * q;
+      reinterpret_cast<uint2*>(o)[0] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+      reinterpret_cast<uint2*>(o + a.C)[0] = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    } else if (MODE == 4) {
+      float f[8];
+      {
+        const uint4 x = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) +
+                                                       sr * a.lds)[q];
+        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          f[2 * e] = __uint_as_float(wv[e] << 16);
+          f[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+        }
+      }
+      uint32_t w[4];
+      bool over = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        over |= fabsf(f[2 * e]) > 65504.0f || fabsf(f[2 * e + 1]) > 65504.0f;
+        w[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(f[2 * e]))) |
+               (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(f[2 * e + 1]))) << 16);
+      }
+      if (over && a.status) atomicOr(a.status, TWELL_FLAG_RANGE);
+      reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(i) * a.ldo)[q] =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (MODE == 2) {
       const float4* s =
           reinterpret_cast<const float4*>(static_cast<const float*>(a.src) + sr * a.lds) + 2 * q;
       const float4 x0 = s[0], x1 = s[1];
@@ -563,9 +606,34 @@ twell_status transpose_run(int mode, const TransposeArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
+namespace {
+__global__ void __launch_bounds__(256) amax_kernel(const float4* src, int64_t n4, uint32_t* out) {
+  uint32_t m = 0u;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = src[i];
+    m = max(m, max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
+                   max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w)))));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(out, m);
+}
+}  // namespace
+
+twell_status amax_run(const float* src, int64_t n, uint32_t* out, cudaStream_t s) {
+  if (cudaMemsetAsync(out, 0, sizeof(uint32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
+  const int64_t n4 = n / 4;
+  if (n4 <= 0) return TWELL_OK;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks > 1216) blocks = 1216;  // 8 per SM
+  amax_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const float4*>(src), n4,
+                                                       out);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
 twell_status gather_run(int mode, const GatherArgs& a, cudaStream_t s) {
   if (a.R <= 0) return TWELL_OK;
-  const long long per_row = mode == 1 ? a.C / 4 : a.C / 8;
+  const long long per_row = (mode == 1 || mode == 3) ? a.C / 4 : a.C / 8;
   long long blocks = (static_cast<long long>(a.R) * per_row + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
@@ -575,6 +643,10 @@ twell_status gather_run(int mode, const GatherArgs& a, cudaStream_t s) {
     gather_kernel<1><<<static_cast<int>(blocks), 256, 0, s>>>(a);
   else if (mode == 2)
     gather_kernel<2><<<static_cast<int>(blocks), 256, 0, s>>>(a);
+  else if (mode == 3)
+    gather_kernel<3><<<static_cast<int>(blocks), 256, 0, s>>>(a);
+  else if (mode == 4)
+    gather_kernel<4><<<static_cast<int>(blocks), 256, 0, s>>>(a);
   else
     return TWELL_ERR_INVALID;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;

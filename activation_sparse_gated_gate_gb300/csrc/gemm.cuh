@@ -99,6 +99,12 @@ twell_status transpose_run(int mode, const TransposeArgs& a, cudaStream_t s);
 //   MODE 0  bf16 rows of C elements (C % 8 == 0), out pitch ldo
 //   MODE 1  fp32 rows split into bf16 [hi (C) | lo (C)], out pitch ldo
 //   MODE 2  fp32 rows rounded to bf16 (C % 8 == 0), out pitch ldo
+//   MODE 3  fp32 rows -> fp16 [hi | lo] (C % 4 == 0), out pitch ldo >= 2C;
+//           with amax set the rows are first multiplied by the power-of-two
+//           gradient scale of scale.cuh
+//   MODE 4  bf16 rows converted to fp16 (C % 8 == 0), out pitch ldo
+//   (modes 3 and 4 set TWELL_FLAG_RANGE in *status, when given, for a value
+//   beyond the fp16 range)
 // With pad > 0, rows R_act <= i < min(R, R_act rounded up to pad) are
 // written as zeros.
 struct GatherArgs {
@@ -110,7 +116,15 @@ struct GatherArgs {
   uint16_t* out;
   int64_t ldo;
   int32_t pad;
+  int32_t* status;
+  const uint32_t* amax;
+  float amax_floor;
 };
 twell_status gather_run(int mode, const GatherArgs& a, cudaStream_t s);
+
+// *out = the bits of max_i |src[i]| over n floats (n % 4 == 0, src 16-byte
+// aligned); NaN compares above every number.  Two launches (a clear, then a
+// grid-stride maximum with one atomic per warp).
+twell_status amax_run(const float* src, int64_t n, uint32_t* out, cudaStream_t s);
 
 }  // namespace twell

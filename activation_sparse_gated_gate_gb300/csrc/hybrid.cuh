@@ -8,8 +8,10 @@ namespace twell {
 
 struct WsLayout {
   size_t bytes = 0;
-  // tensor-core ELL path: gathered bf16 x / dy rows, bf16 ELL values
-  size_t xe = 0, dye = 0, ae = 0, ale = 0, dze = 0, dzl = 0, due = 0;
+  // tensor-core ELL path: gathered x / dy rows, fp16 ELL values and
+  // weights, the gradient scale's maximum
+  size_t xe = 0, dye = 0, ae = 0, dze = 0, dzl = 0, due = 0, wg16 = 0, wu16 = 0, wd16 = 0,
+         amax = 0;
   // forward
   size_t xo = 0, wdT = 0, asplit = 0;
   // backward
@@ -42,13 +44,16 @@ inline WsLayout ws_layout(int op, int64_t T, int64_t D, int64_t F, int64_t cap,
   if (op == 3 || op == 4) {
     w.xe = ws_take(&cur, T * D * 2);
     w.ae = ws_take(&cur, T * n_t * cap * 2);
+    w.wd16 = ws_take(&cur, F * D * 2);
   }
   if (op == 4) {
-    w.dye = ws_take(&cur, T * 2 * D * 2);  // bf16 [hi | lo] rows
-    w.ale = ws_take(&cur, T * n_t * cap * 2);
+    w.dye = ws_take(&cur, T * 2 * D * 2);  // fp16 [hi | lo] rows
     w.dze = ws_take(&cur, T * n_t * cap * 2);
     w.dzl = ws_take(&cur, T * n_t * cap * 2);
     w.due = ws_take(&cur, T * n_t * cap * 2);
+    w.wg16 = ws_take(&cur, F * D * 2);
+    w.wu16 = ws_take(&cur, F * D * 2);
+    w.amax = ws_take(&cur, 4);
   }
   if (op == 1 || op == 3) {
     w.xo = ws_take(&cur, max_dense * D * 2);

@@ -6,29 +6,31 @@
 //
 // ELL rows, forward:
 //   Xe = x[ell rows] (bf16 gather)
-//   SAMPLE_U   u = Xe W_u at the ELL entries -> u_ell, a = bf16(h u)
-//   ROWS       y[ell rows] = E(a) W_d
-// ELL rows, backward:
-//   Xe = x[ell rows] (bf16), dYe = dy[ell rows] split into bf16 hi | lo
-//             (rows up to the next multiple of 64 zero-filled: the K tail of
-//             TRANS)
-//   SAMPLE_DA  da = dYe_hi W_d^T + dYe_lo W_d^T at the entries -> dz = da u +
-//              lambda (bf16 hi and lo), du = da h, a = h u (bf16)
-//   ROWS       dx[ell rows] = E(dz_hi) W_g^T + E(dz_lo) W_g^T + E(du) W_u^T
-//   TRANS x3   dW_g^T = E(dz_hi)^T Xe + E(dz_lo)^T Xe, dW_u^T = E(du)^T Xe,
-//              dW_d = E(a_hi)^T dYe_hi + E(a_lo)^T dYe_hi + E(a_hi)^T dYe_lo
-// dy and dz keep their low halves: a column of W_g with large entries for
-// every neuron (a bias feature) sums dz into dx, where a single bf16
-// rounding of each term would dominate the column's error, and dz = da u is
-// the most heavy-tailed of the sparse values (a product of two roughly
-// normal factors), so in dW_g a few large terms can carry the rounding of
-// an element.  In dW_d both factors are activations; their low halves (the
-// a_lo dy_lo product is below fp32 resolution and left out) keep the
-// heavy-tailed terms that dominate some elements from carrying a bf16
-// rounding each.
-// E(v) = the ELL values expanded to dense bf16 tiles in shared memory.
-// Dense overflow rows: the shared tensor-core path with hi/lo splits, which
-// writes its dx rows and adds its weight-gradient terms after TRANS.
+//   SAMPLE_U   u = Xe W_u at the ELL entries -> u_ell, a = fp16(h u)
+//   ROWS       y[ell rows] = E(a) W_d16                         (fp16 operands)
+// ELL rows, backward (every operand fp16; s = the power-of-two gradient
+// scale of scale.cuh, from max(max |dy|, 2^-14 lambda)):
+//   Xe = fp16(x[ell rows]), dYe = s dy[ell rows] as fp16 hi | lo (rows up
+//             to the next multiple of 64 zero-filled: the K tail of TRANS)
+//   SAMPLE_DA  s da = dYe_hi W_d16^T + dYe_lo W_d16^T at the entries ->
+//              s dz = s da u + s lambda (fp16 hi and lo), s du = s da h, a = h u
+//   ROWS       dx[ell rows] = (E(s dz_hi) W_g16^T + E(s dz_lo) W_g16^T +
+//              E(s du) W_u16^T) / s
+//   TRANS x3   dW_g^T = E(s dz)^T Xe / s, dW_u^T = E(s du)^T Xe / s,
+//              dW_d = E(a)^T dYe_hi / s
+// E(v) = the ELL values expanded to dense fp16 tiles in shared memory;
+// W_*16 = fp16 copies of the weights, made in the workspace by each call.
+// fp16 rounds each operand to 2^-11 relative (bf16: 2^-8) over a range that
+// covers activations and weights and, after the scaling, gradients; a value
+// that leaves it sets TWELL_FLAG_RANGE.  A single fp16 segment per product
+// replaces the bf16 hi + lo pairs a bf16 operand needs for the same error,
+// except on the way to dx: a column of W_g with large entries for every
+// neuron (a bias feature) sums a token's dz into one element of dx, where
+// even fp16's rounding of each term, or the rounding of the token's dy that
+// every da of the token shares, can reach a few percent of dx's RMS, so dz
+// (in dx) and dy (in da) keep fp16 low halves (2^-22).
+// Dense overflow rows: the shared tensor-core path with bf16 hi/lo splits,
+// which writes its dx rows and adds its weight-gradient terms after TRANS.
 #include "hybrid.cuh"
 #include "gemm.cuh"
 #include "tc_ell.cuh"
@@ -48,8 +50,12 @@ twell_status tc_common_checks(const hybrid_t* h, int32_t D, int32_t* T_out) {
 }
 
 twell_status gather_rows(int mode, const void* src, const hybrid_t* h, int32_t D, uint16_t* out,
-                         cudaStream_t s) {
+                         cudaStream_t s, int32_t* status = nullptr,
+                         const uint32_t* amax = nullptr, float amax_floor = 0.0f) {
   GatherArgs g{};
+  g.status = status;
+  g.amax = amax;
+  g.amax_floor = amax_floor;
   g.src = src;
   g.lds = D;
   g.row_idx = h->ell_rows;
@@ -57,7 +63,7 @@ twell_status gather_rows(int mode, const void* src, const hybrid_t* h, int32_t D
   g.C = D;
   g.R_dyn = h->n_ell;
   g.out = out;
-  g.ldo = mode == 1 ? 2 * static_cast<int64_t>(D) : D;
+  g.ldo = mode == 3 ? 2 * static_cast<int64_t>(D) : D;
   g.pad = 64;
   return gather_run(mode, g, s);
 }
@@ -106,9 +112,12 @@ extern "C" twell_status hybrid_ffn_fwd_tc(const uint16_t* x, const hybrid_t* h,
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint16_t* Xe = reinterpret_cast<uint16_t*>(w + L.xe);
   uint16_t* Ae = reinterpret_cast<uint16_t*>(w + L.ae);
+  uint16_t* Wd16 = reinterpret_cast<uint16_t*>(w + L.wd16);
+  const size_t FD = static_cast<size_t>(F) * D;
 
+  if ((st = twell_to_f16(Wd, Wd16, FD, status_dev, s)) != TWELL_OK) return st;
   if ((st = gather_rows(0, x, h, D, Xe, s)) != TWELL_OK) return st;
-  {  // u at the ELL entries, a = bf16(h u)
+  {  // u at the ELL entries, a = fp16(h u)
     TcMaps m;
     if ((st = tc_map_a(&m.a[0], Xe, T, D)) != TWELL_OK) return st;
     if ((st = tc_map_w_kmajor(&m.b[0], Wu_t, F, D)) != TWELL_OK) return st;
@@ -117,12 +126,13 @@ extern "C" twell_status hybrid_ffn_fwd_tc(const uint16_t* x, const hybrid_t* h,
     a.a_ell = Ae;
     if ((st = tc_run(m, a, dev, s)) != TWELL_OK) return st;
   }
-  {  // y[ell rows] = E(a) W_d
+  {  // y[ell rows] = E(a) W_d16
     TcMaps m;
     if ((st = tc_map_cols(&m.cols, h->ell_col, T, n_t, C, 128)) != TWELL_OK) return st;
     if ((st = tc_map_vals(&m.vals[0], Ae, T, n_t, C, 128)) != TWELL_OK) return st;
-    if ((st = tc_map_mn(&m.b[0], Wd, F, D)) != TWELL_OK) return st;
+    if ((st = tc_map_mn(&m.b[0], Wd16, F, D)) != TWELL_OK) return st;
     TcArgs a = tc_args(TC_ROWS, h, D, status_dev);
+    a.f16_ops = 1;
     a.out = y;
     a.ldo = D;
     a.row_idx = h->ell_rows;
@@ -171,41 +181,55 @@ extern "C" twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h,
   uint16_t* Xe = reinterpret_cast<uint16_t*>(w + L.xe);
   uint16_t* dYe = reinterpret_cast<uint16_t*>(w + L.dye);
   uint16_t* Ae = reinterpret_cast<uint16_t*>(w + L.ae);
-  uint16_t* Al = reinterpret_cast<uint16_t*>(w + L.ale);
   uint16_t* dZe = reinterpret_cast<uint16_t*>(w + L.dze);
   uint16_t* dZl = reinterpret_cast<uint16_t*>(w + L.dzl);
   uint16_t* dUe = reinterpret_cast<uint16_t*>(w + L.due);
-  const int64_t D2 = 2 * static_cast<int64_t>(D);
+  uint16_t* Wg16 = reinterpret_cast<uint16_t*>(w + L.wg16);
+  uint16_t* Wu16 = reinterpret_cast<uint16_t*>(w + L.wu16);
+  uint16_t* Wd16 = reinterpret_cast<uint16_t*>(w + L.wd16);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(w + L.amax);
+  const size_t FD = static_cast<size_t>(F) * D;
+  const float floor_v = l1_coeff * 0x1p-14f;  // s lambda < 2^14
 
-  if ((st = gather_rows(0, x, h, D, Xe, s)) != TWELL_OK) return st;
-  if ((st = gather_rows(1, dy, h, D, dYe, s)) != TWELL_OK) return st;
-  {  // da at the ELL entries -> dz (hi, lo), du, a
+  if ((st = twell_to_f16(Wg_t, Wg16, FD, status_dev, s)) != TWELL_OK) return st;
+  if ((st = twell_to_f16(Wu_t, Wu16, FD, status_dev, s)) != TWELL_OK) return st;
+  if ((st = twell_to_f16(Wd, Wd16, FD, status_dev, s)) != TWELL_OK) return st;
+  if ((st = amax_run(dy, static_cast<int64_t>(T) * D, amax, s)) != TWELL_OK) return st;
+  if ((st = gather_rows(4, x, h, D, Xe, s, status_dev)) != TWELL_OK) return st;
+  if ((st = gather_rows(3, dy, h, D, dYe, s, status_dev, amax, floor_v)) != TWELL_OK) return st;
+  const int64_t D2 = 2 * static_cast<int64_t>(D);
+  {  // s da at the ELL entries -> s dz, s du, a
     TcMaps m;
     if ((st = tc_map_a(&m.a[0], dYe, T, D, D2)) != TWELL_OK) return st;
     if ((st = tc_map_a(&m.a[1], dYe + D, T, D, D2)) != TWELL_OK) return st;
-    if ((st = tc_map_w_kmajor(&m.b[0], Wd, F, D)) != TWELL_OK) return st;
+    if ((st = tc_map_w_kmajor(&m.b[0], Wd16, F, D)) != TWELL_OK) return st;
     TcArgs a = tc_args(TC_SAMPLE_DA, h, D, status_dev);
     a.nseg = 2;
+    a.f16_ops = 1;
+    a.amax = amax;
+    a.amax_floor = floor_v;
     a.u_ell = const_cast<float*>(u_ell);
     a.a_ell = Ae;
-    a.a_lo_ell = Al;
     a.dz_ell = dZe;
     a.dz_lo_ell = dZl;
     a.du_ell = dUe;
     a.lambda = l1_coeff;
     if ((st = tc_run(m, a, dev, s)) != TWELL_OK) return st;
   }
-  {  // dx[ell rows] = E(dz_hi) W_g^T + E(dz_lo) W_g^T + E(du) W_u^T
+  {  // dx[ell rows] = (E(s dz_hi) W_g16^T + E(s dz_lo) W_g16^T + E(s du) W_u16^T) / s
     TcMaps m;
-    if ((st = tc_map_mn(&m.b[0], Wg_t, F, D)) != TWELL_OK) return st;
-    if ((st = tc_map_mn(&m.b[1], Wg_t, F, D)) != TWELL_OK) return st;
-    if ((st = tc_map_mn(&m.b[2], Wu_t, F, D)) != TWELL_OK) return st;
+    if ((st = tc_map_mn(&m.b[0], Wg16, F, D)) != TWELL_OK) return st;
+    if ((st = tc_map_mn(&m.b[1], Wg16, F, D)) != TWELL_OK) return st;
+    if ((st = tc_map_mn(&m.b[2], Wu16, F, D)) != TWELL_OK) return st;
     if ((st = tc_map_cols(&m.cols, h->ell_col, T, n_t, C, 128)) != TWELL_OK) return st;
     const uint16_t* segv[3] = {dZe, dZl, dUe};
     for (int q = 0; q < 3; ++q)
       if ((st = tc_map_vals(&m.vals[q], segv[q], T, n_t, C, 128)) != TWELL_OK) return st;
     TcArgs a = tc_args(TC_ROWS, h, D, status_dev);
     a.nseg = 3;
+    a.f16_ops = 1;
+    a.amax = amax;
+    a.amax_floor = floor_v;
     a.out = dx;
     a.ldo = D;
     a.row_idx = h->ell_rows;
@@ -213,24 +237,21 @@ extern "C" twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h,
   }
   {  // weight gradients of the ELL rows (overwrite)
     struct Job {
-      int nseg;
-      const uint16_t* vals[3];
-      const uint16_t* b[3];
+      const uint16_t* vals;
+      const uint16_t* b;
       int64_t pitch;
       float* out;
     };
-    const Job jobs[3] = {{2, {dZe, dZl, nullptr}, {Xe, Xe, nullptr}, D, dWg_t},
-                         {1, {dUe, nullptr, nullptr}, {Xe, nullptr, nullptr}, D, dWu_t},
-                         {3, {Ae, Al, Ae}, {dYe, dYe, dYe + D}, D2, dWd}};
+    const Job jobs[3] = {{dZe, Xe, D, dWg_t}, {dUe, Xe, D, dWu_t}, {Ae, dYe, D2, dWd}};
     for (const Job& jb : jobs) {
       TcMaps m;
       TcArgs a = tc_args(TC_TRANS, h, D, status_dev);
-      a.nseg = jb.nseg;
+      a.f16_ops = 1;
+      a.amax = amax;
+      a.amax_floor = floor_v;
       if ((st = tc_map_cols(&m.cols, h->ell_col, T, n_t, C, 64)) != TWELL_OK) return st;
-      for (int q = 0; q < jb.nseg; ++q) {
-        if ((st = tc_map_mn(&m.b[q], jb.b[q], T, D, jb.pitch)) != TWELL_OK) return st;
-        if ((st = tc_map_vals(&m.vals[q], jb.vals[q], T, n_t, C, 64)) != TWELL_OK) return st;
-      }
+      if ((st = tc_map_mn(&m.b[0], jb.b, T, D, jb.pitch)) != TWELL_OK) return st;
+      if ((st = tc_map_vals(&m.vals[0], jb.vals, T, n_t, C, 64)) != TWELL_OK) return st;
       a.out = jb.out;
       a.ldo = D;
       if ((st = tc_run(m, a, dev, s)) != TWELL_OK) return st;

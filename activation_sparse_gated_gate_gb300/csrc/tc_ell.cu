@@ -10,13 +10,13 @@
 //   warps 2-5   epilogue, one TMEM lane quarter each, two accumulators in
 //               flight
 //   warps 6-21  (expanded modes) four groups of four warps, taking the stages
-//               in turn, write the bf16 A tile of a stage from the raw ELL
+//               in turn, write the fp16 A tile of a stage from the raw ELL
 //               slots: zero it and scatter the entries whose column falls in
 //               the K block, then fence to the async proxy and arrive.  They
 //               issue no global loads of their own, so the proxy fence has no
 //               loads in flight to wait for.
 //   warp 22     (expanded modes) TMA producer of the raw ELL slots (columns
-//               and bf16 values of the rows of the stage) into a ring of
+//               and fp16 values of the rows of the stage) into a ring of
 //               their own, freed by the expansion warps: the raw data runs
 //               ahead of the A/B stages, which the MMA frees.
 // Shared-memory stages: [A 16 KB][B 32 KB] x 4, plus the raw ring (ROWS:
@@ -30,9 +30,10 @@
 //
 // Every wait is bounded (about a second); a wait that runs out sets
 // TWELL_FLAG_TIMEOUT and the CTA leaves its loops, frees its TMEM and exits.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
+#include "scale.cuh"
 #include "tc_ell.cuh"
 
 namespace twell {
@@ -63,8 +64,10 @@ struct TcCfg {
       STAGES * STAGE_BYTES + STAGING + RAW_SLOTS * RAW_SLOT + 512 + 1024;
 };
 
-__device__ __forceinline__ uint16_t bf16_bits(float v) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+// fp16 bits of v; a |v| beyond the fp16 range sets TWELL_FLAG_RANGE
+__device__ __forceinline__ uint16_t f16_bits(float v, int32_t* status) {
+  if (fabsf(v) > 65504.0f) atomicOr(status, TWELL_FLAG_RANGE);
+  return __half_as_ushort(__float2half_rn(v));
 }
 
 // Per-unit decomposition shared by every role.  Returns 0 (nothing to do),
@@ -190,7 +193,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, !Cfg::SAMPLE);
+      const uint32_t idesc = p.f16_ops ? ptx::idesc_f16_f32(BM, BN, false, !Cfg::SAMPLE)
+                                   : ptx::idesc_bf16_f32(BM, BN, false, !Cfg::SAMPLE);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -384,6 +388,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const float lambda_s =
+        p.amax ? p.lambda * pow2_scale(p.amax, p.amax_floor, false) : p.lambda;
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint8_t* my_stage = staging + r * 128;
@@ -482,19 +488,16 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
                 const size_t pos = base + sidx;
                 if (MODE == TC_SAMPLE_U) {
                   p.u_ell[pos] = val;
-                  p.a_ell[pos] = bf16_bits(hv[sidx] * val);
+                  p.a_ell[pos] = f16_bits(hv[sidx] * val, p.status);
                 } else {
-                  const float dz = fmaf(val, uv[sidx], p.lambda);
-                  const uint16_t dz_hi = bf16_bits(dz);
+                  const float dz = fmaf(val, uv[sidx], lambda_s);
+                  const uint16_t dz_hi = f16_bits(dz, p.status);
                   p.dz_ell[pos] = dz_hi;
-                  p.dz_lo_ell[pos] =
-                      bf16_bits(dz - __uint_as_float(static_cast<uint32_t>(dz_hi) << 16));
-                  p.du_ell[pos] = bf16_bits(val * hv[sidx]);
-                  const float a = hv[sidx] * uv[sidx];
-                  const uint16_t a_hi = bf16_bits(a);
-                  p.a_ell[pos] = a_hi;
-                  p.a_lo_ell[pos] =
-                      bf16_bits(a - __uint_as_float(static_cast<uint32_t>(a_hi) << 16));
+                  if (p.dz_lo_ell)
+                    p.dz_lo_ell[pos] = __half_as_ushort(
+                        __float2half_rn(dz - __half2float(__ushort_as_half(dz_hi))));
+                  p.du_ell[pos] = f16_bits(val * hv[sidx], p.status);
+                  p.a_ell[pos] = f16_bits(hv[sidx] * uv[sidx], p.status);
                 }
               }
             }
@@ -511,6 +514,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
           orow = m_blk * BM + r;
         }
         float* o = p.out + orow * p.ldo + n_blk * BN;
+        const float osc = p.amax ? pow2_scale(p.amax, p.amax_floor, true) : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           if (n_blk * BN + c * 32 >= p.D) break;  // uniform
@@ -521,8 +525,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
             float4* o4 = reinterpret_cast<float4*>(o + c * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+              o4[j] = make_float4(osc * __uint_as_float(v[4 * j]),
+                                  osc * __uint_as_float(v[4 * j + 1]),
+                                  osc * __uint_as_float(v[4 * j + 2]),
+                                  osc * __uint_as_float(v[4 * j + 3]));
           }
         }
       }

@@ -5,10 +5,10 @@
 //
 // A variant of the CUDA-core ELL kernels for the dense activation regimes of
 // training, where every 128-token block touches every neuron tile: the ELL
-// values are expanded tile by tile in shared memory into bf16 MMA operands,
+// values are expanded tile by tile in shared memory into fp16 MMA operands,
 // and the dense-to-sparse products are full tcgen05 tiles of which only the
-// ELL entries are kept.  Operands in bf16 (the sparse values rounded once),
-// fp32 accumulation in TMEM.
+// ELL entries are kept.  Operands in bf16 or fp16 (the sparse values written
+// as fp16), fp32 accumulation in TMEM.
 #pragma once
 
 #include "common.cuh"
@@ -17,19 +17,19 @@ namespace twell {
 
 enum TcMode : int32_t {
   // acc = X_ell W_u (M = ELL rows, N = F, K = D); at the ELL entries (i, j):
-  // u_ell = acc, a_ell = bf16(h acc)
+  // u_ell = acc, a_ell = fp16(h acc)
   TC_SAMPLE_U = 0,
   // acc = sum_s dY_s W_d^T (M = ELL rows, N = F, K = D per segment; the
-  // segments are the bf16 hi and lo halves of dy); at the entries:
-  // du = acc h, dz = acc u + lambda, a = h u -> dz_ell (hi) + dz_lo_ell (lo),
-  // du_ell, a_ell (hi) + a_lo_ell (lo) (bf16)
+  // segments are the fp16 hi and lo halves of s dy); at the entries, in
+  // fp16: du = acc h, dz = acc u + s lambda (hi in dz_ell and, when
+  // dz_lo_ell is set, lo), a = h u
   TC_SAMPLE_DA = 1,
   // out[row_idx[i]][:] = sum_s E_s[i][:] W_s (M = ELL rows, N = D, K = F per
   // segment, up to 3 segments), E_s = ELL values vals_s expanded to dense
-  // bf16 rows, W_s [F][D]
+  // fp16 rows, W_s [F][D]
   TC_ROWS = 2,
   // out[j][:] = sum_s sum_i E_s[i][j] B_s[i][:] (M = F, N = D, K = ELL rows
-  // per segment), E_s the ELL values vals_s expanded, B_s [rows][D] bf16 (the
+  // per segment), E_s the ELL values vals_s expanded, B_s [rows][D] fp16 (the
   // gathered x or dy rows)
   TC_TRANS = 3
 };
@@ -37,11 +37,11 @@ enum TcMode : int32_t {
 constexpr int kTcMaxSeg = 3;
 
 struct TcMaps {
-  CUtensorMap a[2];             // SAMPLE: dense bf16 A [rows][D] per segment, box 64 x 128
+  CUtensorMap a[2];             // SAMPLE: dense A [rows][D] per segment, box 64 x 128
   CUtensorMap b[kTcMaxSeg];     // SAMPLE: W [F][D] box 64 x 256 (b[0], every segment);
                                 // ROWS / TRANS: [K][D] box 64 x 64 per segment
   CUtensorMap cols;             // ROWS / TRANS: u8 ELL columns [rows][n_t C], box C x (128|64)
-  CUtensorMap vals[kTcMaxSeg];  // ROWS / TRANS: bf16 ELL values [rows][n_t C] per segment
+  CUtensorMap vals[kTcMaxSeg];  // ROWS / TRANS: fp16 ELL values [rows][n_t C] per segment
 };
 
 struct TcArgs {
@@ -55,12 +55,20 @@ struct TcArgs {
   const uint8_t* ell_cnt;
   const float* ell_val;
   float* u_ell;            // SAMPLE_U out, SAMPLE_DA in
-  uint16_t* a_ell;         // bf16 h u, out of both
-  uint16_t* a_lo_ell;      // SAMPLE_DA out: bf16(h u - bf16(h u))
-  uint16_t* dz_ell;        // SAMPLE_DA out: bf16(dz)
-  uint16_t* dz_lo_ell;     // SAMPLE_DA out: bf16(dz - bf16(dz))
-  uint16_t* du_ell;        // SAMPLE_DA out
+  uint16_t* a_ell;         // fp16 h u, out of both
+  uint16_t* dz_ell;        // SAMPLE_DA out: fp16(dz)
+  uint16_t* dz_lo_ell;     // SAMPLE_DA out (optional): fp16(dz - fp16(dz))
+  uint16_t* du_ell;        // SAMPLE_DA out: fp16(du)
   float lambda;
+  // The A and B tiles of every segment are fp16 (else bf16).  The values the
+  // SAMPLE epilogues write are fp16 either way; one beyond the fp16 range
+  // sets TWELL_FLAG_RANGE.
+  int32_t f16_ops;
+  // Gradient scaling (scale.cuh), when amax is set: SAMPLE_DA's accumulator
+  // is s da (dy scaled by s), and it writes s dz = acc u + s lambda and
+  // s du = acc h; ROWS and TRANS multiply their accumulators by 1 / s.
+  const uint32_t* amax;
+  float amax_floor;
   // ROWS / TRANS epilogues
   float* out;
   int64_t ldo;

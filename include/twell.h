@@ -309,12 +309,19 @@ twell_status hybrid_ffn_bwd(const uint16_t* x, const hybrid_t* h, const float* u
  *   dense-to-sparse products (u, and da in the backward) are full tensor-core
  *   tiles X_ell W_u and dY_ell W_d^T of which only the ELL entries are kept;
  *   sparse-to-dense products (y, dx, dW_g^T, dW_u^T, dW_d) expand the ELL
- *   values tile by tile in shared memory into bf16 operands.
- * The sparse values h u (in y) and du enter the tensor cores rounded to bf16
- * (relative error up to 2^-8 each); dy (in da and dW_d), dz (in dx and
- * dW_g) and h u (in dW_d) are split into bf16 hi and lo halves.
- * Accumulation is fp32; results differ from the CUDA-core entry points by
- * that rounding.  Requires
+ *   values tile by tile in shared memory into fp16 operands.
+ * Apart from x and W_u in u (bf16, exact), every tensor-core operand of the
+ * ELL rows is fp16 (relative rounding up to 2^-11): h u, W_d in y; and in
+ * the backward x, the weights and, multiplied by a power of two s that puts
+ * max(max |dy|, 2^-14 l1_coeff) in [0.5, 1), dy, dz and du (the fp32
+ * products are divided by s again, which rounds nothing); dy in da and dz in
+ * dx also carry an fp16 low half (a bias-like column of W_g sums a token's
+ * dz, and every da of a token shares the token's dy rounding, into one
+ * element of dx).  Weights and the
+ * gathered rows are converted into the workspace by each call.  A value
+ * beyond the fp16 range sets TWELL_FLAG_RANGE (the results are then not
+ * meaningful).  Accumulation is fp32; results differ from the CUDA-core
+ * entry points by that rounding.  Requires
  * D % 64 == 0 and C in {16, 32}; other shapes return TWELL_ERR_UNSUPPORTED.
  * Deterministic for the ELL rows (no atomics); dense rows as above.
  *   ws: twell_workspace_size(TWELL_WS_HYBRID_FWD_TC / _BWD_TC, ...) bytes.

@@ -4,12 +4,12 @@ the dense fp64 oracle.
 
 Bars: the spec bar, max-abs <= 2e-2 * RMS(reference) per tensor, and
 a statistical bug-catching bar, RMS(error) <= 5e-3 * RMS(reference).  The
-variant feeds the sparse values (h u, dz, du) and dy to the tensor cores as
-bf16, each with a relative rounding error below 2^-8 (about 1.7e-3 RMS for
-uniformly spread mantissas), so a product of a few such factors summed over
-many independent terms has an error RMS of a few 1e-3 of the result's RMS;
-a wrong index, sign or dropped term gives errors of the order of the RMS
-itself."""
+variant feeds the sparse values (h u, dz, du), the weights, x and dy to the
+tensor cores as fp16 (dy, dz and du multiplied by a power-of-two gradient
+scale), each with a relative rounding error below 2^-11, so a product of a
+few such factors summed over many independent terms has an error RMS well
+below 1e-3 of the result's RMS; a wrong index, sign, scale or dropped term
+gives errors of the order of the RMS itself."""
 import numpy as np
 import pytest
 import torch
@@ -126,11 +126,15 @@ def test_tc_all_rows_dense():
 @pytest.mark.parametrize("lam", [2e-5, 1.0])
 def test_tc_l1_term_alone(lam):
     # dy = 0: da = 0, so dz = lambda exactly and du = 0 at every active
-    # entry: dx_t = lambda sum_{active j} W_g[:, j] (dz's hi + lo halves),
-    # dW_g^T[j] = lambda sum_{active t} x_t with bf16(lambda) in the ELL
-    # rows (relative error <= 2^-8 on each term, so |err| <= 2^-8 lambda
-    # sum_t |x_t| elementwise: ELL and dense-row terms may cancel in the
-    # reference), dW_u = dW_d = 0 exactly
+    # entry: dx_t = lambda sum_{active j} W_g[:, j], dW_g^T[j] = lambda
+    # sum_{active t} x_t.  The ELL rows carry fp16(s lambda) (one relative
+    # rounding <= 2^-11 shared by every term; s a power of two) and fp16
+    # copies of W_g and x (exact for magnitudes >= 2^-14, else an absolute
+    # error <= 2^-25), the dense rows bf16 hi + lo halves, and fp32 sums add
+    # at most about 2^-15 relative over these term counts, so |err| <= 2^-10
+    # lambda sum |terms| + 2^-24 lambda (number of terms) elementwise (ELL
+    # and dense-row terms may cancel in the reference); dW_u = dW_d = 0
+    # exactly
     w = _training(400, 128, 1024, 0.05, 0.05, 0.4, 16, seed=11)
     r = _run(w, 400, lam, dy=np.zeros_like(w.dy))
     got = r["grads"]
@@ -139,7 +143,8 @@ def test_tc_l1_term_alone(lam):
                               active=act > 0)
     X = oracle.bf16_to_f64(w.x)
     G = oracle.bf16_to_f64(w.Wg_t)
-    bounds = (2.0 ** -16 * lam * (act @ np.abs(G)), 2.0 ** -8 * lam * (act.T @ np.abs(X)))
+    bounds = (2.0 ** -10 * lam * (act @ np.abs(G)) + 2.0 ** -24 * lam * act.sum(1)[:, None],
+              2.0 ** -10 * lam * (act.T @ np.abs(X)) + 2.0 ** -24 * lam * act.sum(0)[:, None])
     for g, rf, b, n in zip(got[:2], ref[:2], bounds, NAMES[:2]):
         err = np.abs(g - rf)
         assert (err <= b + 1e-5 * np.max(np.abs(rf))).all(), n
@@ -156,7 +161,7 @@ def test_tc_lambda_zero_is_plain_gradient():
 
 def test_tc_agrees_with_cuda_core_path():
     # both entry points on the same hybrid: same dense rows (identical
-    # code), ELL rows within the bf16 operand rounding of each other
+    # code), ELL rows within the fp16 operand rounding of each other
     w = _training(600, 256, 1024, 0.05, 0.03, 0.4, 32, seed=13)
     d, h, hyb, z = _hybrid(w, 128)
     dyt = torch.from_numpy(w.dy).cuda()
@@ -176,6 +181,37 @@ def test_tc_agrees_with_cuda_core_path():
     np.testing.assert_allclose(outs[1][0][dense], outs[0][0][dense], rtol=1e-5, atol=1e-5)
     for a, b, n in zip(outs[0][2:], outs[1][2:], NAMES):
         assert rms(a - b) <= 5e-3 * rms(a), n
+
+
+@pytest.mark.parametrize("c,lam", [(1e-12, 0.0), (1e-12, 2e-17), (1e-10, 2e-5), (1e3, 2e-5)])
+def test_tc_gradient_scale(c, lam):
+    # dy far below fp16's normal range (a loss averaged over many tokens),
+    # far above it (where unscaled dz = da u + lambda would overflow fp16),
+    # or far below the L1 coefficient (the scale then follows 2^-14 lambda
+    # and dy scales to below [0.5, 1)): the power-of-two scale keeps every
+    # fp16 operand in range, so the same bars hold for every gradient,
+    # including dW_u and dW_d, which depend on dy alone
+    w = _training(500, 128, 1024, 0.05, 0.05, 0.4, 16, seed=14)
+    dy = (w.dy.astype(np.float64) * c).astype(np.float32)
+    r = _run(w, 128, lam, dy=dy)
+    ref = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, dy, lam, active=r["zg"] > 0)
+    _bars(r["grads"], ref, NAMES)
+
+
+def test_tc_fp16_range_flag():
+    # x multiplied by 2^20: u and h u grow past fp16's 65504 in the forward,
+    # and x itself in the backward's fp16 copy; both calls report it
+    w = _training(256, 128, 512, 0.05, 0.0, 0.4, 16, seed=15)
+    d, h, hyb, z = _hybrid(w, 64)
+    xb = d["x"] * 2.0 ** 20
+    y, u_ell, U_dense = tw.hybrid_ffn_fwd_tc(xb, hyb, d["Wu_t"], d["Wd"])
+    torch.cuda.synchronize()
+    assert int(hyb.status.item()) & tw.FLAG_RANGE
+    hyb.status.zero_()
+    tw.hybrid_ffn_bwd_tc(xb, hyb, u_ell, U_dense, d["Wg_t"], d["Wu_t"], d["Wd"],
+                         torch.from_numpy(w.dy).cuda(), 2e-5)
+    torch.cuda.synchronize()
+    assert int(hyb.status.item()) & tw.FLAG_RANGE
 
 
 def test_tc_unsupported_shapes():
