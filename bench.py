@@ -615,82 +615,116 @@ def run_ours(args, w):
         raise RuntimeError(f"tensor-core and CUDA-core forwards differ (relative {rel:.2e})")
 
     # end to end through the public API with host buffers: pinned x in, y out.
-    # The batch is cut into E_CHUNKS token chunks on three streams (copy in,
-    # compute, copy out) so one chunk's copies overlap another chunk's
-    # kernels; every byte of both copies is inside the timed region, which
-    # runs from before the first copy-in to after the last copy-out.
-    E_CHUNKS = 4
+    # The batch is cut into token chunks on three streams (copy in, compute,
+    # copy out) so one chunk's copies overlap another chunk's kernels; every
+    # byte of both copies is inside the timed region, which runs from before
+    # the first copy-in to after the last copy-out.  The step is bound by
+    # the first copy-in, the sum of the chunks' compute and the copies that
+    # follow the last compute: short first and last chunks shorten the ends,
+    # few chunks keep the per-chunk fixed costs down.  Each candidate plan
+    # (fractions of the batch) runs each chunk on the forward measured
+    # faster at its size; the fastest plan is then timed.
     xh = x.cpu().pin_memory()
     yh = torch.empty_like(y, device="cpu").pin_memory()
-    bounds = [w.T * c // E_CHUNKS for c in range(E_CHUNKS + 1)]
-    hs = [tw.TwELL(bounds[c + 1] - bounds[c], w.F, w.width, device=dev)
-          for c in range(E_CHUNKS)]
-    wss = [torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC, bounds[c + 1] - bounds[c],
-                                                w.D, w.F, 0, 0),), dtype=torch.uint8, device=dev)
-           for c in range(E_CHUNKS)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    plans = {"4 equal": (1, 1, 1, 1), "1:3:3:1": (1, 3, 3, 1), "1:8:5:2": (1, 8, 5, 2),
+             "4:7:4:1": (4, 7, 4, 1)}
 
-    # the chunks are E_CHUNKS times smaller than the batch: time both
-    # forwards once at the chunk size and pipeline the faster
-    def _chunk_ms(fwd_tc):
-        c_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        for it in range(4):
-            if it == 1:
-                c_ev[0].record(stream)
-            for c in range(E_CHUNKS):
+    def plan_sizes(parts):
+        # chunk sizes in whole 128-token blocks, proportional to `parts`
+        blocks = (w.T + 127) // 128
+        cuts = [blocks * sum(parts[:i]) // sum(parts) for i in range(len(parts) + 1)]
+        sizes = [min(w.T, 128 * cuts[i + 1]) - min(w.T, 128 * cuts[i])
+                 for i in range(len(parts))]
+        return [n for n in sizes if n > 0]
+
+    chunk_state = {}
+
+    def chunk_bufs(n):
+        # a TwELL and a tensor-core workspace per chunk (sized for n tokens)
+        h_c = tw.TwELL(n, w.F, w.width, device=dev)
+        ws_c = torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC, n, w.D, w.F, 0, 0),),
+                           dtype=torch.uint8, device=dev)
+        return h_c, ws_c
+
+    def chunk_fwd(a, b, hc, fwd_tc, st):
+        tw.twell_gate_pack(x[a:b], Wg, hc[0], stream=st)
+        if fwd_tc:
+            tw.twell_ffn_fwd_tc(x[a:b], hc[0], Wu, Wd, y=y[a:b], ws=hc[1], Wd_f16=Wd16,
+                                stream=st)
+        else:
+            tw.twell_ffn_fwd(x[a:b], hc[0], Wu, Wd, y=y[a:b], stream=st)
+
+    def chunk_ms(n, fwd_tc):
+        # one chunk of n tokens, device-resident, mean of 3 after a warm-up
+        key = (n, fwd_tc)
+        if key not in chunk_state:
+            hc = chunk_bufs(n)
+            c_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            for it in range(4):
+                if it == 1:
+                    c_ev[0].record(stream)
+                chunk_fwd(0, n, hc, fwd_tc, stream)
+            c_ev[1].record(stream)
+            torch.cuda.synchronize()
+            chunk_state[key] = c_ev[0].elapsed_time(c_ev[1]) / 3
+        return chunk_state[key]
+
+    def use_tc_for(n):
+        if args.forward != "auto":
+            return args.forward == "tc"
+        return chunk_ms(n, True) <= chunk_ms(n, False)
+
+    def build_plan(parts):
+        sizes = plan_sizes(parts)
+        bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
+        bufs = [chunk_bufs(n) for n in sizes]
+        fwds = [use_tc_for(n) for n in sizes]
+
+        def pipelined_step(origin):
+            # fork from `origin`, one chunk per stage on each stream, join back
+            for st in (s_in, s_cmp, s_out):
+                st.wait_stream(origin)
+            for c in range(len(sizes)):
                 a, b = bounds[c], bounds[c + 1]
-                tw.twell_gate_pack(x[a:b], Wg, hs[c], stream=stream)
-                if fwd_tc:
-                    tw.twell_ffn_fwd_tc(x[a:b], hs[c], Wu, Wd, y=y[a:b], ws=wss[c],
-                                        Wd_f16=Wd16, stream=stream)
-                else:
-                    tw.twell_ffn_fwd(x[a:b], hs[c], Wu, Wd, y=y[a:b], stream=stream)
-        c_ev[1].record(stream)
+                with torch.cuda.stream(s_in):
+                    x[a:b].copy_(xh[a:b], non_blocking=True)
+                s_cmp.wait_stream(s_in)
+                with torch.cuda.stream(s_cmp):
+                    chunk_fwd(a, b, bufs[c], fwds[c], s_cmp)
+                s_out.wait_stream(s_cmp)
+                with torch.cuda.stream(s_out):
+                    yh[a:b].copy_(y[a:b], non_blocking=True)
+            origin.wait_stream(s_out)
+
+        # one pipelined step recorded as a CUDA graph: replaying it costs one
+        # host call, so the step is not bound by per-call host overhead
+        pipelined_step(stream)
         torch.cuda.synchronize()
-        return c_ev[0].elapsed_time(c_ev[1])
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            pipelined_step(cap)
+        torch.cuda.synchronize()
+        return {"sizes": sizes, "fwds": fwds, "bufs": bufs, "graph": graph}
 
-    chunk_tc = (_chunk_ms(True) <= _chunk_ms(False) if args.forward == "auto"
-                else args.forward == "tc")
+    def replay_ms(plan, n):
+        e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            e_ev[i][0].record(stream)
+            plan["graph"].replay()
+            e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in e_ev]
 
-    def pipelined_step(origin):
-        # fork from `origin`, one chunk per stage on each stream, join back
-        for st in (s_in, s_cmp, s_out):
-            st.wait_stream(origin)
-        for c in range(E_CHUNKS):
-            a, b = bounds[c], bounds[c + 1]
-            with torch.cuda.stream(s_in):
-                x[a:b].copy_(xh[a:b], non_blocking=True)
-            s_cmp.wait_stream(s_in)
-            with torch.cuda.stream(s_cmp):
-                tw.twell_gate_pack(x[a:b], Wg, hs[c], stream=s_cmp)
-                if chunk_tc:
-                    tw.twell_ffn_fwd_tc(x[a:b], hs[c], Wu, Wd, y=y[a:b], ws=wss[c], Wd_f16=Wd16,
-                                        stream=s_cmp)
-                else:
-                    tw.twell_ffn_fwd(x[a:b], hs[c], Wu, Wd, y=y[a:b], stream=s_cmp)
-            s_out.wait_stream(s_cmp)
-            with torch.cuda.stream(s_out):
-                yh[a:b].copy_(y[a:b], non_blocking=True)
-        origin.wait_stream(s_out)
-
-    # one pipelined step recorded as a CUDA graph: replaying it costs one host
-    # call, so the step is not bound by per-call host overhead
-    pipelined_step(stream)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.graph(graph, stream=cap):
-        pipelined_step(cap)
-    torch.cuda.synchronize()
-    e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    for i in range(K):
-        flush.zero_()
-        e_ev[i][0].record(stream)
-        graph.replay()
-        e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e_ev) / K, dev)
+    built = {name: build_plan(parts) for name, parts in plans.items()}
+    trial = {name: statistics.median(replay_ms(pl, 5)) for name, pl in built.items()}
+    plan_name = min(trial, key=trial.get)
+    plan = built[plan_name]
+    e2e_ms = max_over_ranks(sum(replay_ms(plan, K)) / K, dev)
+    hs = [b[0] for b in plan["bufs"]]
     if any(int(hh.status.item()) for hh in hs):
         raise RuntimeError("device status flags set in the end-to-end run")
     if not torch.equal(yh.to(dev), y):
@@ -782,10 +816,14 @@ def run_ours(args, w):
                    "parallelism": f"replicas x{ws}"},
         "e2e": {"value": job_tokens_per_s(w.T, ws, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "pipeline": (f"{E_CHUNKS} token chunks, copy-in / compute / copy-out streams, "
-                             "replayed as one CUDA graph"),
-                "forward": ("tensor-core union gather" if chunk_tc
-                            else "CUDA-core fused kernel") + " (the faster at the chunk size)"},
+                "pipeline": (f"token chunks {plan['sizes']} (plan {plan_name}, the fastest of "
+                             f"{len(plans)} tried untimed), copy-in / compute / copy-out "
+                             "streams, replayed as one CUDA graph"),
+                "forward": [("tensor-core" if f else "CUDA-core") for f in plan["fwds"]],
+                "forward_choice": ("per chunk, the faster measured at its size"
+                                   if args.forward == "auto"
+                                   else f"fixed by --forward {args.forward}"),
+                "plans_tried_ms": trial},
         # our kernels in the timed region per iteration: gate, union scan, up
         # and down GEMMs (headline) + gate and fused kernel (CUDA-core step)
         "gpu_launches": 6 * K,
