@@ -20,9 +20,10 @@ __all__ = [
     "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
     "twell_ffn_fwd_tc", "twell_to_f16",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
-    "hybrid_ffn_bwd",
+    "hybrid_ffn_bwd", "hybrid_ffn_fwd_tc", "hybrid_ffn_bwd_tc",
     "twell_status_string",
     "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "TILE",
+    "WS_HYBRID_FWD", "WS_HYBRID_BWD", "WS_HYBRID_FWD_TC", "WS_HYBRID_BWD_TC", "WS_FFN_FWD_TC",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
