@@ -271,6 +271,16 @@ def _block_unions(h, T, F):
     return int(np.unpackbits(bits).sum())
 
 
+def plan_sizes(T, parts):
+    """Token chunk sizes of the end-to-end pipeline: whole 128-token blocks
+    (the last chunk may end in a partial block) in proportion to `parts`,
+    summing to T, empty chunks dropped."""
+    blocks = (T + 127) // 128
+    cuts = [blocks * sum(parts[:i]) // sum(parts) for i in range(len(parts) + 1)]
+    sizes = [min(T, 128 * cuts[i + 1]) - min(T, 128 * cuts[i]) for i in range(len(parts))]
+    return [n for n in sizes if n > 0]
+
+
 def fma_peak_tflops(sm_count, sm_mhz):
     """FP32 FMA peak: 128 FP32 lanes per SM (4 sub-partitions x 32), 2 flops
     per FMA, at the given SM clock."""
@@ -630,14 +640,6 @@ def run_ours(args, w):
     plans = {"4 equal": (1, 1, 1, 1), "1:3:3:1": (1, 3, 3, 1), "1:8:5:2": (1, 8, 5, 2),
              "4:7:4:1": (4, 7, 4, 1)}
 
-    def plan_sizes(parts):
-        # chunk sizes in whole 128-token blocks, proportional to `parts`
-        blocks = (w.T + 127) // 128
-        cuts = [blocks * sum(parts[:i]) // sum(parts) for i in range(len(parts) + 1)]
-        sizes = [min(w.T, 128 * cuts[i + 1]) - min(w.T, 128 * cuts[i])
-                 for i in range(len(parts))]
-        return [n for n in sizes if n > 0]
-
     chunk_state = {}
 
     def chunk_bufs(n):
@@ -676,7 +678,7 @@ def run_ours(args, w):
         return chunk_ms(n, True) <= chunk_ms(n, False)
 
     def build_plan(parts):
-        sizes = plan_sizes(parts)
+        sizes = plan_sizes(w.T, parts)
         bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
         bufs = [chunk_bufs(n) for n in sizes]
         fwds = [use_tc_for(n) for n in sizes]

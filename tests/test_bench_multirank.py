@@ -44,3 +44,16 @@ def test_max_over_ranks_and_job_value_two_ranks():
 def test_single_process_identity():
     assert bench.max_over_ranks(1.25) == 1.25
     assert bench.job_tokens_per_s(100, 1, 10.0) == pytest.approx(1e4)
+
+
+@pytest.mark.parametrize("T", [1, 64, 128, 1000, 8192, 8200, 16384])
+@pytest.mark.parametrize("parts", [(1, 1, 1, 1), (1, 3, 3, 1), (1, 8, 5, 2), (4, 7, 4, 1)])
+def test_pipeline_plan_sizes(T, parts):
+    # the end-to-end pipeline's chunks cover the batch once, in order, and
+    # every chunk but the last starts and ends on a 128-token block boundary
+    sizes = bench.plan_sizes(T, parts)
+    assert sum(sizes) == T and all(n > 0 for n in sizes)
+    assert all(n % 128 == 0 for n in sizes[:-1])
+    assert len(sizes) <= len(parts)
+    if T == 8192:
+        assert sizes == [8192 * p // sum(parts) for p in parts]
