@@ -198,6 +198,40 @@ def test_tc_gradient_scale(c, lam):
     _bars(r["grads"], ref, NAMES)
 
 
+def _random_cases(n, seed=2026):
+    # seeded shapes: ragged T, D a multiple of 64, any tile count, both
+    # capacities, with and without dense rows, three L1 coefficients and dy
+    # spread over 15 decades (the gradient scale's range)
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        c = dict(T=int(rng.integers(64, 2600)), D=int(rng.choice([64, 128, 192, 256, 320, 512])),
+                 F=128 * int(rng.integers(2, 17)), C=int(rng.choice([16, 32])),
+                 p=float(rng.uniform(0.02, 0.09)), frac=float(rng.choice([0.0, 0.02, 0.08])),
+                 pd=float(rng.uniform(0.35, 0.5)), lam=float(rng.choice([0.0, 2e-5, 1e-3])),
+                 sc=float(10 ** rng.uniform(-12, 3)), seed=len(out) + 100)
+        try:
+            workloads.make_training("check", c["T"], c["D"], c["F"], c["p"], c["frac"], c["pd"],
+                                    c["C"], c["lam"], seed=c["seed"])
+        except ValueError:  # no base density gives the mean
+            continue
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("c", _random_cases(6), ids=lambda c: f"T{c['T']}D{c['D']}F{c['F']}C{c['C']}")
+def test_tc_random_shapes(c):
+    w = workloads.make_training("check", c["T"], c["D"], c["F"], c["p"], c["frac"], c["pd"],
+                                c["C"], c["lam"], seed=c["seed"])
+    dy = (w.dy.astype(np.float64) * c["sc"]).astype(np.float32)
+    r = _run(w, w.T, c["lam"], dy=dy)
+    act = r["zg"] > 0
+    y_ref = oracle.ffn_forward(w.x, w.Wg_t, w.Wu_t, w.Wd, active=act)
+    _bars([r["y"].cpu().numpy().astype(np.float64)], [y_ref], ("y",))
+    ref = oracle.ffn_backward(w.x, w.Wg_t, w.Wu_t, w.Wd, dy, c["lam"], active=act)
+    _bars(r["grads"], ref, NAMES)
+
+
 def test_tc_fp16_range_flag():
     # x multiplied by 2^20: u and h u grow past fp16's 65504 in the forward,
     # and x itself in the backward's fp16 copy; both calls report it
