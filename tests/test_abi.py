@@ -115,3 +115,31 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("has a GPU")
     assert _pack(lib, _struct()) in (CUDA, UNSUPPORTED)
+
+
+def test_workspace_sizes(lib):
+    # every workspace covers the buffers its entry point carves out of it
+    # (each rounded up to 256 bytes), and bad arguments give 0
+    T, D, F, C, MD = 1000, 256, 1024, 32, 64
+    n_t = F // tw.TILE
+    ell = T * n_t * C * 2            # one fp16 / bf16 value per ELL slot
+    fd = F * D * 2                   # one 16-bit copy of a weight matrix
+    fwd_tc = tw.twell_workspace_size(tw.WS_HYBRID_FWD_TC, T, D, F, C, MD)
+    bwd_tc = tw.twell_workspace_size(tw.WS_HYBRID_BWD_TC, T, D, F, C, MD)
+    fwd_cc = tw.twell_workspace_size(tw.WS_HYBRID_FWD, T, D, F, C, MD)
+    # x rows + a + fp16 W_d, plus the dense-row buffers of the CUDA-core forward
+    assert fwd_tc >= T * D * 2 + ell + fd + fwd_cc - 3 * 256
+    # x rows, dy hi | lo rows, a, dz hi and lo, du, three fp16 weight copies
+    assert bwd_tc >= T * D * 2 + T * 2 * D * 2 + 4 * ell + 3 * fd
+    assert tw.twell_workspace_size(tw.WS_FFN_FWD_TC, 8192, 1536, 6144, 0, 0) >= \
+        2 * (8192 + 1536) * 6144
+    for op in (tw.WS_HYBRID_FWD, tw.WS_HYBRID_BWD, tw.WS_HYBRID_FWD_TC, tw.WS_HYBRID_BWD_TC):
+        assert tw.twell_workspace_size(op, T, D, F, C, MD) > 0
+        assert tw.twell_workspace_size(op, -1, D, F, C, MD) == 0
+        assert tw.twell_workspace_size(op, T, 0, F, C, MD) == 0
+        assert tw.twell_workspace_size(op, T, D, F, 0, MD) == 0
+        assert tw.twell_workspace_size(op, T, D, F, C, -1) == 0
+    assert tw.twell_workspace_size(0, T, D, F, C, MD) == 0
+    assert tw.twell_workspace_size(6, T, D, F, C, MD) == 0
+    # T = 0 needs no per-row buffers but stays a valid request
+    assert tw.twell_workspace_size(tw.WS_HYBRID_BWD_TC, 0, D, F, C, MD) >= 3 * fd
