@@ -10,8 +10,13 @@
 // code cannot use the variable's name as a device address (on the host it
 // names a stand-in), so the first call on each device asks the runtime for
 // the array's device address with cudaGetSymbolAddress, with that device
-// current, and caches it; that first call should therefore come before any
-// stream capture.  All calls share the one array and it keeps the contents
+// current, and caches it together with the device's current context; that
+// first call should therefore come before any stream capture.  A context
+// torn down and created again (cudaDeviceReset, or the primary context
+// released and retained) reloads the library's module at another address,
+// so a call that finds a different current context looks the address up
+// again (that call, too, should not be made under stream capture).  All
+// calls share the one array and it keeps the contents
 // of the last call; hybrid_ffn_fwd writes every workspace byte it later
 // reads, so nothing has to start at zero.  Calls that may overlap on the GPU
 // (different streams, or different host threads) race on the array.
@@ -29,6 +34,28 @@ __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+CUcontext g_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
+
+// The calling thread's current context (driver API, reached through the
+// runtime's entry-point query so the library does not link libcuda), or
+// nullptr if it cannot be read.
+CUcontext current_context() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+  });
+  CUcontext c = nullptr;
+  if (g_ctx_get == nullptr || g_ctx_get(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 }  // namespace
 }  // namespace twell
@@ -55,11 +82,15 @@ extern "C" twell_status hybrid_ffn_fwd_noalloc(const uint16_t* x, const hybrid_t
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_addr[dev] == nullptr) {
+    const CUcontext ctx = current_context();
+    if (g_addr[dev] == nullptr || ctx == nullptr || ctx != g_ctx[dev]) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
         return TWELL_ERR_CUDA;
       g_addr[dev] = p;
+      // the lookup makes the device's primary context current if the thread
+      // had none yet, so the context is read again after it
+      g_ctx[dev] = current_context();
     }
     scratch = g_addr[dev];
   }

@@ -102,8 +102,18 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
   const size_t src_rt = static_cast<size_t>(t) * p.n_t;
   const size_t dst_rt = static_cast<size_t>(i) * p.n_t;
   for (int k = lane; k < p.n_t; k += 32) {
-    const int c = p.cnt[src_rt + k];  // <= C for an ELL row
-    p.ell_cnt[dst_rt + k] = static_cast<uint8_t>(c);
+    int c = min(static_cast<int>(p.cnt[src_rt + k]), p.C);  // <= C for an ELL row
+    int slot = -1;
+    if (c > p.W) {
+      slot = p.spill_slot[src_rt + k];
+      if (slot < 0 || slot >= p.spill_cap) {
+        // the gate kernel found no room for this slice: the tile is stored
+        // empty (count 0, every slot padding) so that no reader follows a
+        // column the slots do not hold
+        if (p.status) atomicOr(p.status, TWELL_FLAG_SPILL_FULL);
+        c = 0;
+      }
+    }
     float* dv = p.ell_val + (dst_rt + k) * p.C;
     uint8_t* dc = p.ell_col + (dst_rt + k) * p.C;
     // padding slots: column sentinel 0xff (whole rows of 16 bytes first,
@@ -114,21 +124,16 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
     } else {
       for (int s = c; s < p.C; ++s) dc[s] = 0xffu;
     }
-    if (c <= p.W) {
+    int s = 0;
+    if (c > 0 && c <= p.W) {
       const float* sv = p.val + (src_rt + k) * p.W;
       const uint8_t* sc = p.col + (src_rt + k) * p.W;
-      for (int s = 0; s < c; ++s) {
+      for (; s < c; ++s) {
         dv[s] = sv[s];
         dc[s] = sc[s];
       }
-    } else {
-      const int slot = p.spill_slot[src_rt + k];
-      if (slot < 0 || slot >= p.spill_cap) {
-        if (p.status) atomicOr(p.status, TWELL_FLAG_SPILL_FULL);
-        continue;
-      }
+    } else if (c > 0) {
       const float* sl = p.spill_val + static_cast<size_t>(slot) * TWELL_TILE;
-      int s = 0;
       for (int cc = 0; cc < TWELL_TILE && s < c; ++cc) {
         const float v = sl[cc];
         if (v > 0.0f) {
@@ -137,7 +142,12 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
           ++s;
         }
       }
+      // a slice with fewer positive values than its count leaves the rest
+      // of its slots as padding
+      for (int r = s; r < c; ++r) dc[r] = 0xffu;
     }
+    // the count is the number of entries written, stored last
+    p.ell_cnt[dst_rt + k] = static_cast<uint8_t>(s);
   }
 }
 

@@ -232,7 +232,10 @@ typedef struct {
  * TwELL to the hybrid format).  Reads the TwELL `h` (slots and spill) and
  * fills `out` (out->T == h->T, out->F == h->F; C = out->cap may differ from
  * h->width: entries beyond W come from the spill slices).  Row lists and
- * counts are produced on the device; nothing is read back.
+ * counts are produced on the device; nothing is read back.  A (row, tile)
+ * that needs its spill slice when the TwELL's spill list had no room for it
+ * is stored empty (ELL count 0, every slot padding; zeros in a dense row)
+ * and TWELL_FLAG_SPILL_FULL is set.
  */
 twell_status twell_to_hybrid(const twell_t* h, const hybrid_t* out, int32_t* status_dev,
                              void* stream);
@@ -348,8 +351,12 @@ twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h, const float
  *   forward workspace (twell_workspace_size(TWELL_WS_HYBRID_FWD, ...)) is
  *   larger returns TWELL_ERR_UNSUPPORTED and enqueues nothing.
  *   The first call on a device looks up the array's device address (with
- *   that device current) and caches it; make that first call before any
- *   stream capture.  The entry point allocates nothing.
+ *   that device current) and caches it with the device's current context;
+ *   make that first call before any stream capture.  After the context is
+ *   destroyed and created again (cudaDeviceReset), the array lives at a new
+ *   address: the next call sees the new context and looks it up again, so
+ *   it too belongs outside stream capture.  The entry point allocates
+ *   nothing.
  *   All calls share the array: calls that may overlap on the GPU race.
  */
 twell_status hybrid_ffn_fwd_noalloc(const uint16_t* x, const hybrid_t* h, const uint16_t* Wu_t,

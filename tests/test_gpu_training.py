@@ -79,6 +79,54 @@ def test_to_hybrid_dense_capacity_exhausted_sets_flag():
     _assert_hybrid_equal(hyb, ref, 4)
 
 
+def test_to_hybrid_spill_list_exhausted_stores_empty_tiles():
+    # C > W, so ELL rows take entries beyond W from the spill slices, and the
+    # spill list holds only 200 of them: every (row, tile) whose slice is
+    # missing must come out as an empty tile (count 0, all padding), the rest
+    # as the oracle packs them; the forwards then read only stored entries.
+    w = workloads.make_training("spill-exhausted", 640, 128, 1024, 0.08, 0.05, 0.5, 16,
+                                2e-5, seed=41)
+    w.width = 8
+    d, h, z = run_pack(w, spill_cap=200)
+    hyb = tw.Hybrid(w.T, w.F, 16, w.T)
+    tw.twell_to_hybrid(h, hyb)
+    torch.cuda.synchronize()
+    assert int(h.spill_n.item()) > 200
+    assert int(hyb.status.item()) & tw.FLAG_SPILL_FULL
+    zg = z.cpu().numpy()
+    ref = oracle.to_hybrid(oracle.twell_pack(zg, 128, w.width), 16)
+    cnt_g = h.cnt.cpu().numpy().astype(np.int64)
+    slot = h.spill_slot.cpu().numpy()
+    lost = (cnt_g > w.width) & ((slot < 0) | (slot >= 200))   # (t, k) without a slice
+    n_ell = hyb.n_ell
+    assert n_ell == len(ref.ell_rows)
+    ell_lost = lost[ref.ell_rows]
+    assert ell_lost.any() and (~ell_lost & (ref.ell_cnt > w.width)).any()
+    cnt = hyb.ell_cnt[:n_ell].cpu().numpy().astype(np.int64)
+    col = hyb.ell_col[:n_ell].cpu().numpy().astype(np.int64)
+    val = hyb.ell_val[:n_ell].cpu().numpy()
+    assert (cnt[ell_lost] == 0).all() and (col[ell_lost] == 0xFF).all()
+    keep = ~ell_lost
+    np.testing.assert_array_equal(cnt[keep], ref.ell_cnt[keep])
+    used = np.arange(16)[None, :] < ref.ell_cnt[keep][:, None]
+    np.testing.assert_array_equal(np.where(used, col[keep], -1),
+                                  np.where(used, ref.ell_col[keep], -1))
+    np.testing.assert_array_equal(np.where(used, val[keep], 0),
+                                  np.where(used, ref.ell_val[keep], 0))
+    # the forwards compute y from what is stored: the gate with the lost
+    # tiles' entries removed (dense rows: their lost tiles read as zeros)
+    act = zg > 0
+    n_t = w.F // 128
+    act.reshape(w.T, n_t, 128)[lost] = False
+    y_ref = oracle.ffn_forward(w.x, w.Wg_t, w.Wu_t, w.Wd, active=act)
+    for fwd in (tw.hybrid_ffn_fwd, tw.hybrid_ffn_fwd_tc):
+        y, _, _ = fwd(d["x"], hyb, d["Wu_t"], d["Wd"])
+        torch.cuda.synchronize()
+        assert int(hyb.status.item()) & ~tw.FLAG_SPILL_FULL == 0
+        err = float(np.abs(y.cpu().numpy().astype(np.float64) - y_ref).max())
+        assert err <= 2e-2 * float(np.sqrt(np.mean(y_ref ** 2))), fwd.__name__
+
+
 # --------------------------------------------------------------- hybrid forward
 
 from _gpu import check_y  # noqa: E402

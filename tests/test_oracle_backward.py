@@ -139,3 +139,76 @@ def test_stack_chain_rule_finite_differences():
                 wm[l][k][j, d] -= eps
                 fd = (loss(X0, wp) - loss(X0, wm)) / (2 * eps)
                 assert abs(fd - grads[l][k][j, d]) <= 1e-5 * max(1.0, abs(fd)), (l, k, j, d)
+
+
+def test_stack_rounded_inputs_straight_through_finite_differences():
+    # round_inputs=True (the default): each layer input is the stream rounded
+    # to bf16 and the backward passes through the rounding as the identity.
+    # Pin: freeze each layer's rounding offset c_l = bf16(x_l) - x_l at the
+    # base point (bf16 by torch's CPU conversion, not the oracle's), so the
+    # layer input is x_l + c_l.  That surrogate equals the rounded stack at
+    # the base point and its exact gradient is the straight-through one, so
+    # the oracle's forward matches it there and its gradients match central
+    # differences of it.
+    import torch
+    rng = np.random.default_rng(31)
+    T, D, F = 4, 8, 16
+
+    def bits(a):
+        return oracle.f32_to_bf16(a.astype(np.float32))
+
+    x = bits(rng.standard_normal((T, D)))
+    layers = [tuple(bits(rng.standard_normal((F, D)) * 0.4) for _ in range(3))
+              for _ in range(3)]
+    dy = rng.standard_normal((T, D))
+    lam = 0.05
+    out, dx0, grads = oracle.stack_forward_backward(x, layers, dy, lam)
+    ws = [[oracle.bf16_to_f64(w) for w in layer] for layer in layers]
+    X0 = oracle.bf16_to_f64(x)
+
+    def torch_bf16(a):
+        return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(
+            torch.float64).numpy()
+
+    # offsets at the base point
+    offs = []
+    X = X0
+    for G, U, Dn in ws:
+        offs.append(torch_bf16(X) - X)
+        y = oracle.ffn_forward_f64(X + offs[-1], G, U, Dn)
+        y[:, -1] = 0.0
+        X = X + y
+    assert np.abs(X - out).max() <= 1e-12 * max(1.0, np.abs(out).max())
+    # at least one layer input really was rounded
+    assert max(np.abs(c).max() for c in offs[1:]) > 0
+
+    def loss(X0, ws):
+        X = X0
+        total = 0.0
+        for (G, U, Dn), c in zip(ws, offs):
+            A = X + c
+            z = A @ G.T
+            total += lam * np.sum(np.where(z > 0, z, 0.0))
+            y = oracle.ffn_forward_f64(A, G, U, Dn)
+            y[:, -1] = 0.0
+            X = X + y
+        return total + float(np.sum(X * dy))
+
+    eps = 1e-6
+    for (t, d) in [(0, 0), (1, 3), (3, 6)]:
+        Xp, Xm = X0.copy(), X0.copy()
+        Xp[t, d] += eps
+        Xm[t, d] -= eps
+        fd = (loss(Xp, ws) - loss(Xm, ws)) / (2 * eps)
+        assert abs(fd - dx0[t, d]) <= 1e-5 * max(1.0, abs(fd))
+    for l in range(3):
+        for k in range(3):
+            for (j, d) in [(0, 0), (7, 2), (15, 6)]:
+                wp = [list(w) for w in ws]
+                wm = [list(w) for w in ws]
+                wp[l][k] = ws[l][k].copy()
+                wm[l][k] = ws[l][k].copy()
+                wp[l][k][j, d] += eps
+                wm[l][k][j, d] -= eps
+                fd = (loss(X0, wp) - loss(X0, wm)) / (2 * eps)
+                assert abs(fd - grads[l][k][j, d]) <= 1e-5 * max(1.0, abs(fd)), (l, k, j, d)
