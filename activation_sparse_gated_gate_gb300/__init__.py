@@ -21,7 +21,7 @@ __all__ = [
     "twell_ffn_fwd_tc", "twell_to_f16",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd", "hybrid_ffn_fwd_tc", "hybrid_ffn_bwd_tc",
-    "twell_status_string",
+    "twell_status_string", "twell_probe_fma",
     "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "TILE",
     "WS_HYBRID_FWD", "WS_HYBRID_BWD", "WS_HYBRID_FWD_TC", "WS_HYBRID_BWD_TC", "WS_FFN_FWD_TC",
 ]
@@ -91,6 +91,8 @@ _SIGNATURES = {
     "hybrid_ffn_fwd_noalloc": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_i32,
                                        c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "twell_status_string": (ctypes.c_char_p, [c_i32]),
+    "twell_probe_fma": (c_i32, [c_i32, c_i32, c_ptr, ctypes.c_size_t,
+                                ctypes.POINTER(ctypes.c_int64), c_ptr]),
     "twell_version": (c_i32, []),
 }
 
@@ -430,3 +432,19 @@ def hybrid_ffn_fwd_noalloc(x, h: Hybrid, Wu_t, Wd, y=None, u_ell=None, U_dense=N
                                             _ptr(status), _stream(stream)),
                "hybrid_ffn_fwd_noalloc")
     return y, u_ell, U_dense
+
+
+def twell_probe_fma(packed: bool, iters: int, out=None, stream=None, device=None):
+    """Launch the FP32 FMA throughput probe (scalar or packed f32x2 chains);
+    returns (out, flops) where flops = 2 * 16 * iters * threads.  The caller
+    times the launch on ``stream``."""
+    device = torch.device(device if device is not None else "cuda")
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+    if out is None:
+        out = torch.empty((2 * n_sm * 512,), dtype=torch.float32, device=device)
+    threads = ctypes.c_int64(0)
+    with torch.cuda.device(device):
+        _check(lib().twell_probe_fma(1 if packed else 0, int(iters), _ptr(out), out.numel(),
+                                     ctypes.byref(threads), _stream(stream)),
+               "twell_probe_fma")
+    return out, 2.0 * 16 * iters * threads.value

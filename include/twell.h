@@ -363,6 +363,20 @@ twell_status hybrid_ffn_fwd_noalloc(const uint16_t* x, const hybrid_t* h, const 
                                     const uint16_t* Wd, int32_t D, float* y, float* u_ell,
                                     float* U_dense, int32_t* status_dev, void* stream);
 
+/*
+ * FP32 FMA throughput probe (a measurement helper; the paper has no
+ * counterpart).  Launches, on `stream`, one grid of two 512-thread CTAs per
+ * SM in which every thread runs 16 independent register-resident chains
+ * acc = acc * a + b for `iters` rounds: scalar fp32 FMAs (packed = 0) or
+ * packed two-lane fma.rn.f32x2 (packed != 0, the form the CUDA-core kernels
+ * use).  The caller times the launch with CUDA events; the work is
+ * 2 * 16 * iters * (*threads) flops.  `out` (device, 16-byte aligned,
+ * out_len >= *threads floats) receives one sum per thread; `*threads` (host)
+ * is set before the launch.  TWELL_ERR_INVALID if out_len is too small.
+ */
+twell_status twell_probe_fma(int32_t packed, int32_t iters, float* out, size_t out_len,
+                             int64_t* threads, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* twell_status_string(twell_status s);
 
