@@ -21,7 +21,7 @@ __all__ = [
     "twell_ffn_fwd_tc", "twell_to_f16",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd", "hybrid_ffn_fwd_tc", "hybrid_ffn_bwd_tc",
-    "twell_status_string", "twell_probe_fma",
+    "twell_status_string", "twell_probe_fma", "twell_gate_pack_wait_limit",
     "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "TILE",
     "WS_HYBRID_FWD", "WS_HYBRID_BWD", "WS_HYBRID_FWD_TC", "WS_HYBRID_BWD_TC", "WS_FFN_FWD_TC",
 ]
@@ -91,6 +91,7 @@ _SIGNATURES = {
     "hybrid_ffn_fwd_noalloc": (c_i32, [c_ptr, ctypes.POINTER(HybridStruct), c_ptr, c_ptr, c_i32,
                                        c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "twell_status_string": (ctypes.c_char_p, [c_i32]),
+    "twell_gate_pack_wait_limit": (ctypes.c_uint64, [ctypes.c_uint64]),
     "twell_probe_fma": (c_i32, [c_i32, c_i32, c_ptr, ctypes.c_size_t,
                                 ctypes.POINTER(ctypes.c_int64), c_ptr]),
     "twell_version": (c_i32, []),
@@ -196,6 +197,12 @@ def twell_gate_pack(x, Wg_t, out: TwELL, z_debug=None, status=None, stream=None)
                                      _ptr(z_debug), _ptr(status), _stream(stream)),
                "twell_gate_pack")
     return out
+
+
+def twell_gate_pack_wait_limit(ns: int) -> int:
+    """Set the bound (ns) on the gate kernel's pipeline waits for later
+    ``twell_gate_pack`` calls (0 = the 1 s default); returns the previous."""
+    return int(lib().twell_gate_pack_wait_limit(int(ns)))
 
 
 def twell_ffn_fwd(x, h: TwELL, Wu_t, Wd, y=None, status=None, stream=None):

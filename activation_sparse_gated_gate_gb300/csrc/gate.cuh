@@ -1,0 +1,20 @@
+// Internal interface between the gate entry point and its decode-size
+// kernel (gate_decode.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace twell {
+
+// True when the decode-size gate kernel handles T tokens of width D
+// (1 <= T <= 256 and at least two K blocks of 64 to split).
+bool gate_decode_supported(int32_t T, int32_t D);
+
+// Enqueue the decode-size gate kernel (the caller has validated the
+// arguments and zeroed out->spill_n and out->block_bits on `s`).
+twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const uint16_t* Wg_t,
+                                int32_t T, int32_t D, int32_t F, const twell_t* out,
+                                float* z_debug, int32_t* status_dev, uint64_t wait_ns,
+                                cudaStream_t s);
+
+}  // namespace twell

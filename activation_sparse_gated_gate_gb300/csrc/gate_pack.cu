@@ -20,7 +20,20 @@
 //               registers already loaded.
 // The accumulator is double-buffered so the epilogue of tile i overlaps the
 // MMAs of tile i+1.
+//
+// Every pipeline wait is bounded (by default about 1 s; twell_gate_pack_
+// wait_limit sets another bound).  A role whose wait runs out sets
+// TWELL_FLAG_TIMEOUT, marks the CTA aborted and leaves its loop; the other
+// roles' waits then run out too.  Before the TMEM is freed, an aborted CTA
+// drains what it already issued: the producer waits for the last TMA load
+// of every stage it filled, the MMA issuer commits to a barrier of its own
+// and waits for all its MMAs; both waits use the fixed 1 s bound.  The
+// epilogue's TMEM loads complete before it moves on, so no copy or MMA is in
+// flight when the CTA deallocates and exits.
+#include <atomic>
+
 #include "common.cuh"
+#include "gate.cuh"
 #include "ptx.cuh"
 
 namespace twell {
@@ -29,6 +42,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
 struct GatePackParams {
   int32_t T, D, F, n_t, W;
@@ -44,6 +60,7 @@ struct GatePackParams {
   uint32_t* block_bits;  // optional [num_m][F / 32]
   float* z_debug;
   int32_t* status;
+  uint64_t wait_ns;  // bound on each pipeline wait
 };
 
 template <int BN, int STAGES>
@@ -59,6 +76,13 @@ struct GateCfg {
 
 __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);
+}
+
+// A pipeline wait under the call's bound (short bounds are checked on every
+// retry, the default one every 64).
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return limit_ns >= kDefaultWaitNs ? ptx::mbar_wait(bar, parity, limit_ns)
+                                    : ptx::mbar_wait_strict(bar, parity, limit_ns);
 }
 
 template <int BN, int STAGES>
@@ -77,6 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile uint32_t* aborted = tmem_slot + 1;
+  uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);
+  uint32_t n_loads = 0;  // TMA stage fills issued (producer thread)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -92,6 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], 128);
     }
+    ptx::mbar_init(drain, 1);
+    *aborted = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -112,8 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m_blk = tile / p.num_n;
         const int n_blk = tile % p.num_n;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
+          if (!pipe_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
             flag(p.status, TWELL_FLAG_TIMEOUT);
+            *aborted = 1u;
             goto done;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
@@ -121,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            m_blk * BM);
           ptx::tma_load_2d(sB + stage * Cfg::B_BYTES, &tmap_w, &full[stage], kb * BK,
                            n_blk * BN);
+          ++n_loads;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -138,15 +169,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
+        if (!pipe_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns)) {
           flag(p.status, TWELL_FLAG_TIMEOUT);
+          *aborted = 1u;
           goto done;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!ptx::mbar_wait(&full[stage], phase)) {
+          if (!pipe_wait(&full[stage], phase, p.wait_ns)) {
             flag(p.status, TWELL_FLAG_TIMEOUT);
+            *aborted = 1u;
             goto done;
           }
           ptx::tc_fence_after();
@@ -180,8 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       // the decision must be warp-uniform: tcgen05.ld below is warp-collective
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
-        if (lane == 0) flag(p.status, TWELL_FLAG_TIMEOUT);
+      if (!__all_sync(0xffffffffu, pipe_wait(&tfull[acc], acc_phase, p.wait_ns))) {
+        if (lane == 0) {
+          flag(p.status, TWELL_FLAG_TIMEOUT);
+          *aborted = 1u;
+        }
         goto done;
       }
       ptx::tc_fence_after();
@@ -292,6 +328,24 @@ done:
   __syncwarp();  // lanes idle during the producer / MMA loops rejoin lane 0
   ptx::tc_fence_before();
   __syncthreads();
+  if (*aborted) {  // read after the barrier: the same value in every thread
+    if (warp == 0 && lane == 0) {
+      // the last fill of each stage: n_loads fills went round the ring in
+      // order, stage s got (n_loads - s + STAGES - 1) / STAGES of them
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t n_s = (n_loads + STAGES - 1 - s) / STAGES;
+        if (n_s > 0 && !ptx::mbar_wait(&full[s], (n_s - 1) & 1u)) break;
+      }
+    }
+    if (warp == 1 && lane == 0) {
+      ptx::tc_fence_after();
+      ptx::mma_commit(drain);  // arrives once every MMA this thread issued is done
+      ptx::mbar_wait(drain, 0);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
@@ -348,6 +402,7 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
   p.block_bits = out->block_bits;
   p.z_debug = z_debug;
   p.status = status_dev;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
 
   if (cudaMemsetAsync(out->spill_n, 0, sizeof(int32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
   if (out->block_bits &&
@@ -355,6 +410,11 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
                       static_cast<size_t>(p.num_m) * (F / 32) * sizeof(uint32_t), s) !=
           cudaSuccess)
     return TWELL_ERR_CUDA;
+
+  // Decode-sized batches: the split-K kernel with the tokens as the MMA's N
+  // (every TwELL tile on a 2-CTA cluster, W_g streamed once).
+  if (gate_decode_supported(T, D))
+    return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, p.wait_ns, s);
 
   // Wide tiles (N = 256, two TwELL tiles per accumulator) when they still
   // give every SM work; N = 128 otherwise (few token rows).
@@ -368,4 +428,8 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
   if ((st = make_tmap_bf16_2d(&mx, x, D, T, BK, BM)) != TWELL_OK) return st;
   if ((st = make_tmap_bf16_2d(&mw, Wg_t, D, F, BK, BN)) != TWELL_OK) return st;
   return wide ? launch<256, 4>(dev, mx, mw, p, s) : launch<128, 6>(dev, mx, mw, p, s);
+}
+
+extern "C" uint64_t twell_gate_pack_wait_limit(uint64_t ns) {
+  return twell::g_wait_ns.exchange(ns == 0 ? twell::kDefaultWaitNs : ns);
 }

@@ -62,7 +62,7 @@ typedef enum {
 enum {
   TWELL_FLAG_SPILL_FULL = 1,  /* more (row, tile) slices overflowed W than spill_cap */
   TWELL_FLAG_DENSE_FULL = 2,  /* more overflow rows than the hybrid's max_dense */
-  TWELL_FLAG_TIMEOUT = 4,     /* a pipeline wait exceeded its bound (about 1 s) */
+  TWELL_FLAG_TIMEOUT = 4,     /* a pipeline wait exceeded its bound (about 1 s by default) */
   TWELL_FLAG_RANGE = 8        /* a value exceeded the fp16 range of an fp16 operand */
 };
 
@@ -128,6 +128,18 @@ typedef struct {
 twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T, int32_t D,
                              int32_t F, const twell_t* out, float* z_debug,
                              int32_t* status_dev, void* stream);
+
+/*
+ * Bound, in nanoseconds, on each pipeline wait of the gate kernel launched
+ * by later twell_gate_pack calls (process-wide; 0 restores the default of
+ * 1e9 ns); returns the previous bound.  A wait that runs out sets
+ * TWELL_FLAG_TIMEOUT; the kernel then waits (up to 1 s each) for the TMA
+ * loads and MMAs it already issued, frees its tensor memory and returns, so
+ * the context stays usable and the TwELL of that call is undefined.  Meant
+ * for exercising that path (the paper has no counterpart); a bound of a
+ * few nanoseconds makes every call time out.
+ */
+uint64_t twell_gate_pack_wait_limit(uint64_t ns);
 
 /*
  * Fused up + down projection from a TwELL gate (paper section 2.B.2): for

@@ -128,6 +128,32 @@ def test_spill_capacity_exhausted_sets_flag():
         np.testing.assert_array_equal(sl, ref.spill[k])
 
 
+@pytest.mark.parametrize("T,D,F", [(300, 4096, 2048),    # narrow tiles, 64 K steps
+                                    (1280, 1024, 4096),   # wide tiles, several per CTA
+                                    (64, 4096, 2048)])    # decode kernel: split-K clusters
+def test_gate_pack_wait_timeout_sets_flag_then_recovers(T, D, F):
+    # A 2 ns bound on the gate kernel's pipeline waits: they run out, the
+    # kernel sets TWELL_FLAG_TIMEOUT, drains the loads and MMAs it issued and
+    # returns; the same call under the default bound then packs exactly.
+    w = workloads.random_small(T, D, F, 0.05, 8, seed=T + 1)
+    d = upload(w)
+    h = tw.TwELL(T, F, 8)
+    torch.cuda.synchronize()
+    prev = tw.twell_gate_pack_wait_limit(2)
+    try:
+        tw.twell_gate_pack(d["x"], d["Wg_t"], h)
+        torch.cuda.synchronize()
+    finally:
+        tw.twell_gate_pack_wait_limit(prev)
+    assert prev == 1_000_000_000
+    assert int(h.status.item()) & tw.FLAG_TIMEOUT
+    _, h2, z = run_pack(w, d)
+    torch.cuda.synchronize()
+    assert int(h2.status.item()) == 0
+    zg = _check_z(w, z)
+    assert_twell_equal(fetch_twell(h2), oracle.twell_pack(zg, 128, 8))
+
+
 def test_empty_batch_is_noop():
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     W = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
