@@ -11,6 +11,7 @@ been built, every call raises.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -22,17 +23,20 @@ __all__ = [
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd", "hybrid_ffn_fwd_tc", "hybrid_ffn_bwd_tc",
     "twell_status_string", "twell_probe_fma", "twell_gate_pack_wait_limit",
-    "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "TILE",
+    "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "FLAG_BOUNDS", "TILE",
+    "library",
     "WS_HYBRID_FWD", "WS_HYBRID_BWD", "WS_HYBRID_FWD_TC", "WS_HYBRID_BWD_TC", "WS_FFN_FWD_TC",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libtwell.so")
+BOUNDS_LIB_PATH = os.path.join(HERE, "libtwell_bounds.so")
 TILE = 128
 FLAG_SPILL_FULL = 1
 FLAG_DENSE_FULL = 2
 FLAG_TIMEOUT = 4
 FLAG_RANGE = 8
+FLAG_BOUNDS = 16
 
 c_i32 = ctypes.c_int32
 c_ptr = ctypes.c_void_p
@@ -98,6 +102,15 @@ _SIGNATURES = {
 }
 
 
+def _load(path):
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib():
     """The loaded ``libtwell.so`` (raises if it has not been built)."""
     global _LIB
@@ -106,13 +119,25 @@ def lib():
             raise RuntimeError(
                 f"{LIB_PATH} is missing: build it with "
                 "`python -m activation_sparse_gated_gate_gb300.build`")
-        handle = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGNATURES.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _LIB = handle
+        _LIB = _load(LIB_PATH)
     return _LIB
+
+
+@contextlib.contextmanager
+def library(path):
+    """Route this binding's calls through another build of the library at
+    ``path`` (e.g. ``BOUNDS_LIB_PATH``, the bounds-checking build) inside
+    the ``with`` block."""
+    global _LIB
+    prev = lib()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m activation_sparse_gated_gate_gb300.build`")
+    _LIB = _load(path)
+    try:
+        yield _LIB
+    finally:
+        _LIB = prev
 
 
 def twell_status_string(code: int) -> str:

@@ -25,6 +25,7 @@
 // sums: x_t and W_u stay bf16, nothing is widened) and a butterfly
 // reduction, and accumulate (h u) W_d[j, :] with the packed fp32-pair FMA
 // (fma.rn.f32x2) on W_d's bf16 pairs widened to fp32 pairs.
+#include "bounds.cuh"
 #include "fused.cuh"
 #include "ptx.cuh"
 
@@ -106,9 +107,11 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
   auto issue = [&](const Entry& e, uint32_t n) {
     const int s = static_cast<int>(n % static_cast<uint32_t>(P));
     uint8_t* dst = stages + static_cast<size_t>(s) * 2 * row_bytes;
+    const size_t j = static_cast<size_t>(
+        clamp_index(e.j, static_cast<long long>(p.n_t) * TWELL_TILE, p.status));
     ptx::mbar_arrive_expect_tx(&bars[s], 2 * row_bytes);
-    ptx::bulk_load(dst, p.Wu_t + static_cast<size_t>(e.j) * D, row_bytes, &bars[s]);
-    ptx::bulk_load(dst + row_bytes, p.Wd + static_cast<size_t>(e.j) * D, row_bytes, &bars[s]);
+    ptx::bulk_load(dst, p.Wu_t + j * D, row_bytes, &bars[s]);
+    ptx::bulk_load(dst + row_bytes, p.Wd + j * D, row_bytes, &bars[s]);
   };
 
   // Each CTA owns a contiguous range of units; its warps take the next unit
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
     // row: index into the count / slot arrays; t: token (x and y row)
     const int row = ELL ? static_cast<int>(u) : static_cast<int>(u / p.upr);
     const int t = ELL ? p.ell_rows[row] : row;
+    if (ELL && !in_bounds(t, p.T, p.status)) continue;  // warp-uniform
     const int k_begin = static_cast<int>(u % p.upr) * p.G;
     const int k_end = min(k_begin + p.G, p.n_t);
     uint32_t xb[NC][4];
@@ -145,7 +149,8 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
     const size_t row_rt = static_cast<size_t>(row) * p.n_t;
     for (int kb = k_begin; kb < k_end; kb += 32) {
       const int k = kb + lane;
-      const int c = k < k_end ? p.cnt[row_rt + k] : 0;
+      int c = k < k_end ? p.cnt[row_rt + k] : 0;
+      if (!in_bounds(c, (ELL ? p.W : TWELL_TILE) + 1, p.status)) c = 0;
       // entries of tile k: its slots, or the positives of its spill slice
       // (the spill holds exactly c positive values)
       int spill = -1;
@@ -249,7 +254,9 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
           float part = ((pp[0] + pp[1]) + (pp[2] + pp[3])) + ((pp[4] + pp[5]) + (pp[6] + pp[7]));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-          if (ELL && lane == 0) p.u_save[e.pos] = part;
+          if (ELL && lane == 0 &&
+              in_bounds(e.pos, static_cast<long long>(p.T) * p.n_t * p.W, p.status))
+            p.u_save[e.pos] = part;
           const float sc = e.h * part;
           const f32x2 sc2 = pack2(sc, sc);
 #pragma unroll

@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "bounds.cuh"
 #include "fused.cuh"
 #include "ptx.cuh"
 #include "tc_ell.cuh"
@@ -150,11 +151,14 @@ template <typename Fn>
 __device__ __forceinline__ void ug_walk_pair(const UgArgs& p, size_t rt, int k, bool flag_missing,
                                              Fn&& fn) {
   const int c = p.cnt[rt];
-  if (c == 0) return;
+  if (c == 0 || !in_bounds(c, TWELL_TILE + 1, p.status)) return;
   if (c <= p.W) {
     const uint8_t* cp = p.col + rt * p.W;
     const float* vp = p.val + rt * p.W;
-    for (int s = 0; s < c; ++s) fn(k * TWELL_TILE + cp[s], vp[s]);
+    for (int s = 0; s < c; ++s) {
+      const int n = k * TWELL_TILE + cp[s];
+      if (in_bounds(n, p.F, p.status)) fn(n, vp[s]);
+    }
   } else {
     const int sl = p.spill_slot[rt];
     if (sl < 0 || sl >= p.spill_cap) {
@@ -373,9 +377,11 @@ __device__ __forceinline__ void walk_tiles(const UgArgs& p, size_t rtb, int k0, 
       }
 #pragma unroll
       for (int e = 0; e < WV; ++e)
-        if (e < cn[b])
-          fn((k + b) * TWELL_TILE + static_cast<int>((cw[b][e >> 2] >> (8 * (e & 3))) & 0xffu),
-             vs[b][e]);
+        if (e < cn[b]) {
+          const int n =
+              (k + b) * TWELL_TILE + static_cast<int>((cw[b][e >> 2] >> (8 * (e & 3))) & 0xffu);
+          if (in_bounds(n, p.F, p.status)) fn(n, vs[b][e]);
+        }
     }
   }
 }
@@ -571,14 +577,18 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           const size_t koff = static_cast<size_t>(kb) * UG_BK + 8 * cj;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            ptx::cp_async16(dst0 + i * 1024, p.Wu_t + static_cast<size_t>(ids[i]) * p.D + koff);
+            ptx::cp_async16(dst0 + i * 1024,
+                            p.Wu_t + static_cast<size_t>(clamp_index(ids[i], p.F, p.status)) * p.D +
+                                koff);
         } else {
           const uint32_t box = sB + ((g >> 3) & 3) * 8192;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int k = (g >> 5) + 2 * i;
-            ptx::cp_async16(box + k * 128 + ((cj ^ (k & 7)) << 4),
-                            p.Wd16 + static_cast<size_t>(ids[i]) * p.D + col, nbytes);
+            ptx::cp_async16(
+                box + k * 128 + ((cj ^ (k & 7)) << 4),
+                p.Wd16 + static_cast<size_t>(clamp_index(ids[i], p.F, p.status)) * p.D + col,
+                nbytes);
           }
           if (kb + UG_ST < U.kb) {
 #pragma unroll

@@ -11,7 +11,8 @@ namespace twell {
 bool gate_decode_supported(int32_t T, int32_t D);
 
 // Enqueue the decode-size gate kernel (the caller has validated the
-// arguments and zeroed out->spill_n and out->block_bits on `s`).
+// arguments and zeroed out->spill_n on `s`; the kernel stores every word of
+// out->block_bits itself).
 twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const uint16_t* Wg_t,
                                 int32_t T, int32_t D, int32_t F, const twell_t* out,
                                 float* z_debug, int32_t* status_dev, uint64_t wait_ns,

@@ -13,13 +13,19 @@
 //   * the MMA is z^T = W_g^T x^T: M = 128 neurons (the W_g tile, K-major by
 //     TMA), N = the tokens rounded up to 16 (the x tile, rows past T read as
 //     zeros), fp32 accumulation in TMEM (lane = neuron, column = token);
+//   * each CTA walks its K blocks from a starting block that differs from
+//     tile to tile (and wraps around), so the loads in flight at any moment
+//     cover many column offsets of W_g instead of one 128-byte segment of
+//     rows exactly 2 D bytes apart, which kept the DRAM at a fifth of its
+//     bandwidth when every CTA walked K in step;
 //   * rank 1 reads its partial sums from TMEM into its (then idle) stage
 //     buffers as token rows; after a cluster barrier rank 0 adds them to its
 //     own through distributed shared memory, writes the sums as token rows
 //     of 128 values into its own stage buffers, and one epilogue thread per
 //     token packs its row into TwELL exactly as the batch kernel does
 //     (ascending slots, true count, fp32 spill slice when the count exceeds
-//     W); the block bitmaps are warp ballots over the neurons.
+//     W); each word of the block bitmaps is one warp's ballot over its 32
+//     neurons, stored by that warp alone (so the bitmap needs no zeroing).
 // Roles per CTA: warp 0 TMA producer, warp 1 TMEM allocation and MMA issue,
 // warps 2-5 epilogue (warp w reads TMEM lanes 32 (w mod 4) .. + 31).
 //
@@ -157,7 +163,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = ptx::cluster_ctarank();
   const int tile = static_cast<int>(blockIdx.x >> 1);
   const int kb0 = rank == 0 ? 0 : p.kb_split;
-  const int kb1 = rank == 0 ? p.kb_split : p.nkb;
+  const int nloc = (rank == 0 ? p.kb_split : p.nkb) - kb0;   // K blocks of this CTA
+  const int rot = nloc > 0 ? (tile * 7 + static_cast<int>(rank) * 3) % nloc : 0;
   const int S = p.stages;
   uint32_t n_loads = 0;  // stage fills issued (producer thread)
 
@@ -187,7 +194,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int i = 0; i < nloc; ++i) {
+        const int kb = kb0 + (i + rot < nloc ? i + rot : i + rot - nloc);
         if (!pipe_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
           flag(p.status, TWELL_FLAG_TIMEOUT);
           *aborted = 1u;
@@ -211,7 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int i = 0; i < nloc; ++i) {
         if (!pipe_wait(&full[stage], phase, p.wait_ns)) {
           flag(p.status, TWELL_FLAG_TIMEOUT);
           *aborted = 1u;
@@ -225,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < DK / 16; ++kk)
           ptx::mma_bf16(tmem_base, ptx::sdesc_kmajor_sw128(a_addr + kk * 32),
                         ptx::sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                        (kb > kb0 || kk > 0) ? 1u : 0u);
+                        (i > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(&empty[stage]);
         if (++stage == S) {
           stage = 0;
@@ -310,10 +318,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (p.block_bits) {
+          // this warp alone produces the word: stored, not OR-ed (no zeroing)
           const uint32_t word = __ballot_sync(0xffffffffu, any);
-          if (lane == 0 && word)
-            atomicOr(p.block_bits + static_cast<size_t>(tb / DM) * (p.F / 32) + tile * 4 + q,
-                     word);
+          if (lane == 0)
+            p.block_bits[static_cast<size_t>(tb / DM) * (p.F / 32) + tile * 4 + q] = word;
         }
         ptx::bar_sync(1, 128);  // the block's rows are staged
         const int t = tb + tl_own;

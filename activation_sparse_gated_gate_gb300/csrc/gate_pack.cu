@@ -405,16 +405,18 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
 
   if (cudaMemsetAsync(out->spill_n, 0, sizeof(int32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
+
+  // Decode-sized batches: the split-K kernel with the tokens as the MMA's N
+  // (every TwELL tile on a 2-CTA cluster, W_g streamed once; it stores every
+  // block-bitmap word itself).
+  if (gate_decode_supported(T, D))
+    return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, p.wait_ns, s);
+
   if (out->block_bits &&
       cudaMemsetAsync(out->block_bits, 0,
                       static_cast<size_t>(p.num_m) * (F / 32) * sizeof(uint32_t), s) !=
           cudaSuccess)
     return TWELL_ERR_CUDA;
-
-  // Decode-sized batches: the split-K kernel with the tokens as the MMA's N
-  // (every TwELL tile on a 2-CTA cluster, W_g streamed once).
-  if (gate_decode_supported(T, D))
-    return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, p.wait_ns, s);
 
   // Wide tiles (N = 256, two TwELL tiles per accumulator) when they still
   // give every SM work; N = 128 otherwise (few token rows).

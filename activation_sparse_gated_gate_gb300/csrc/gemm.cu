@@ -15,6 +15,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "bounds.cuh"
 #include "gemm.cuh"
 #include "ptx.cuh"
 #include "scale.cuh"
@@ -54,6 +55,9 @@ template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int m, int n0,
                                                const uint32_t (&r)[32], bool full) {
   const int N = p.N;
+  if ((EPI == EPI_STORE || EPI == EPI_ADD) && p.row_idx && p.row_limit &&
+      !in_bounds(p.row_idx[m], p.row_limit, p.status))
+    return;
   if ((EPI == EPI_STORE || EPI == EPI_ADD) && p.ksplit > 1) {
     const int64_t row = p.row_idx ? p.row_idx[m] : m;
     float* c = p.C + row * p.ldc + n0;
@@ -424,7 +428,10 @@ __global__ void __launch_bounds__(256) transpose_kernel(const TransposeArgs a) {
     const int c = c0 + tx;
     float v = 0.0f;
     if (r < R_act && c < a.C) {
-      const int64_t sr = a.row_idx ? a.row_idx[r] : r;
+      const int64_t sr =
+          a.row_idx ? (a.row_limit ? clamp_index(a.row_idx[r], a.row_limit, a.status)
+                                   : static_cast<long long>(a.row_idx[r]))
+                    : r;
       if (MODE == 0) {
         v = bf16_val(static_cast<const uint16_t*>(a.src)[sr * a.lds + c]);
       } else {
@@ -475,7 +482,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
       }
       continue;
     }
-    const int64_t sr = a.row_idx ? a.row_idx[i] : i;
+    const int64_t sr =
+        a.row_idx ? (a.row_limit ? clamp_index(a.row_idx[i], a.row_limit, a.status)
+                                 : static_cast<long long>(a.row_idx[i]))
+                  : i;
     if (MODE == 3) {
       const float4 x =
           reinterpret_cast<const float4*>(static_cast<const float*>(a.src) + sr * a.lds)[q];
@@ -570,19 +580,22 @@ int gemm_ksplit(int64_t tiles, int64_t k, const DeviceInfo& dev) {
 namespace {
 __global__ void __launch_bounds__(256) zero_rows_kernel(float* C, int64_t ldc,
                                                         const int32_t* row_idx, int32_t R,
-                                                        const int32_t* R_dyn, int32_t N) {
+                                                        const int32_t* R_dyn, int32_t N,
+                                                        int32_t row_limit, int32_t* status) {
   const int R_act = R_dyn ? min(R, *R_dyn) : R;
   const int i = blockIdx.x;
   if (i >= R_act) return;
+  if (row_idx && row_limit && !in_bounds(row_idx[i], row_limit, status)) return;
   float* row = C + static_cast<int64_t>(row_idx ? row_idx[i] : i) * ldc;
   for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = 0.0f;
 }
 }  // namespace
 
 twell_status zero_rows(float* C, int64_t ldc, const int32_t* row_idx, int32_t R,
-                       const int32_t* R_dyn, int32_t N, cudaStream_t s) {
+                       const int32_t* R_dyn, int32_t N, cudaStream_t s, int32_t row_limit,
+                       int32_t* status) {
   if (R <= 0) return TWELL_OK;
-  zero_rows_kernel<<<R, 256, 0, s>>>(C, ldc, row_idx, R, R_dyn, N);
+  zero_rows_kernel<<<R, 256, 0, s>>>(C, ldc, row_idx, R, R_dyn, N, row_limit, status);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -45,6 +45,8 @@ struct GemmArgs {
   float* C;
   int64_t ldc;
   const int32_t* row_idx;  // STORE / ADD: output row of tile row m (identity when null)
+  int32_t row_limit;       // rows of C that row_idx may name (0: unchecked; checked only
+                           // in the bounds-checking build)
   const float* H;          // [M][N]
   const float* U_in;       // [M][N]
   float* U_out;            // [M][N]
@@ -73,8 +75,11 @@ twell_status gemm_run(const GemmMaps& maps, const GemmArgs& a, bool wide_n,
 int gemm_ksplit(int64_t tiles, int64_t k, const DeviceInfo& dev);
 
 // C[row_idx[i]][0..N) = 0 for i < min(R, *R_dyn).
+// (row_limit: rows of C that row_idx may name, 0 unchecked; checked only in
+// the bounds-checking build, with TWELL_FLAG_BOUNDS in *status)
 twell_status zero_rows(float* C, int64_t ldc, const int32_t* row_idx, int32_t R,
-                       const int32_t* R_dyn, int32_t N, cudaStream_t s);
+                       const int32_t* R_dyn, int32_t N, cudaStream_t s, int32_t row_limit = 0,
+                       int32_t* status = nullptr);
 
 // out_hi[c][r] (and out_lo[c][r]) = transposed, bf16-split value v(r, c) for
 // r < R_act (= min(R, *R_dyn)), zeros for R_act <= r < R_pad, c < C:
@@ -92,6 +97,8 @@ struct TransposeArgs {
   uint16_t* out_hi;
   uint16_t* out_lo;
   int64_t ldo;
+  int32_t row_limit;  // rows of src that row_idx may name (0: unchecked)
+  int32_t* status;    // TWELL_FLAG_BOUNDS in the bounds-checking build
 };
 twell_status transpose_run(int mode, const TransposeArgs& a, cudaStream_t s);
 
@@ -111,6 +118,7 @@ struct GatherArgs {
   const void* src;
   int64_t lds;
   const int32_t* row_idx;
+  int32_t row_limit;  // rows of src that row_idx may name (0: unchecked)
   int32_t R, C;
   const int32_t* R_dyn;
   uint16_t* out;

@@ -29,6 +29,7 @@
 //       device)
 // dW rows are written by `dw` first and accumulated into by G5-G7; dx rows
 // of ELL and dense tokens are written by ell_bwd and G4 respectively.
+#include "bounds.cuh"
 #include "gemm.cuh"
 #include "hybrid.cuh"
 #include "ptx.cuh"
@@ -103,9 +104,13 @@ __global__ void __launch_bounds__(256) count_kernel(const BwdParams p) {
   if (i >= *p.n_ell) return;
   const size_t rt0 = static_cast<size_t>(i) * p.n_t;
   for (int k = lane; k < p.n_t; k += 32) {
-    const int c = p.ell_cnt[rt0 + k];
+    int c = p.ell_cnt[rt0 + k];
+    if (!in_bounds(c, p.C + 1, p.status)) c = 0;
     const uint8_t* col = p.ell_col + (rt0 + k) * p.C;
-    for (int s = 0; s < c; ++s) atomicAdd(&p.cnt[k * TWELL_TILE + col[s]], 1);
+    for (int s = 0; s < c; ++s) {
+      const int j = k * TWELL_TILE + col[s];
+      if (in_bounds(j, p.F, p.status)) atomicAdd(&p.cnt[j], 1);
+    }
   }
 }
 
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
   auto issue = [&](const BEntry& e, uint32_t n) {
     const int s = static_cast<int>(n % static_cast<uint32_t>(P));
     uint8_t* dst = stages + static_cast<size_t>(s) * stage_bytes;
-    const size_t off = static_cast<size_t>(e.j) * D;
+    const size_t off = static_cast<size_t>(clamp_index(e.j, p.F, p.status)) * D;
     ptx::mbar_arrive_expect_tx(&bars[s], stage_bytes);
     ptx::bulk_load(dst, p.Wd + off, row_bytes, &bars[s]);
     ptx::bulk_load(dst + row_bytes, p.Wg_t + off, row_bytes, &bars[s]);
@@ -182,6 +187,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
     const int i = i_begin + __shfl_sync(0xffffffffu, take, 0);
     if (i >= i_end) break;
     const int t = p.ell_rows[i];
+    if (!in_bounds(t, p.T, p.status)) continue;  // warp-uniform
     f32x2 dyf[NC][4];  // dy_t, fp32 pairs
     f32x2 acc[NC][4];  // dx_t accumulator, fp32 pairs
     const float* dyr = p.dy + static_cast<size_t>(t) * D;
@@ -205,7 +211,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
     const size_t rt0 = static_cast<size_t>(i) * p.n_t;
     for (int kb = 0; kb < p.n_t; kb += 32) {
       const int k = kb + lane;
-      const int n = k < p.n_t ? p.ell_cnt[rt0 + k] : 0;
+      int n = k < p.n_t ? p.ell_cnt[rt0 + k] : 0;
+      if (!in_bounds(n, p.C + 1, p.status)) n = 0;
       int off = n;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -259,7 +266,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
           float da = ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
-          const float u = p.u_ell[en.pos];
+          const float u =
+              p.u_ell[clamp_index(en.pos, static_cast<long long>(p.T) * p.n_t * p.C, p.status)];
           const float du = da * en.h;
           const float dz = fmaf(da, u, p.lambda);
           const f32x2 dz2 = pack2(dz, dz);
@@ -278,9 +286,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
               }
             }
           }
-          if (lane == 0) {
+          if (lane == 0 && in_bounds(en.j, p.F, p.status)) {
             const int r = atomicAdd(&p.cursor[en.j], 1);
-            p.rec[r] = BwdRecord{t, dz, du, en.h * u};
+            if (in_bounds(r, static_cast<long long>(p.T) * p.n_t * p.C, p.status))
+              p.rec[r] = BwdRecord{t, dz, du, en.h * u};
           }
           __syncwarp();
           if (lane == 0 && e + P < m) {
@@ -316,13 +325,18 @@ __global__ void __launch_bounds__(384) dw_kernel(const BwdParams p) {
   float g[8], w[8], d[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) g[e] = w[e] = d[e] = 0.0f;
-  const int r0 = p.offs[j];
-  const int r1 = p.offs[j + 1];
+  const long long n_rec = static_cast<long long>(p.T) * p.n_t * p.C;
+  int r0 = p.offs[j];
+  int r1 = p.offs[j + 1];
+  if (!in_bounds(r0, n_rec + 1, p.status) || !in_bounds(r1, n_rec + 1, p.status) || r1 < r0)
+    r0 = r1 = 0;
   if (own) {
     int r = r0;
     for (; r + 2 <= r1; r += 2) {
-      const BwdRecord a = p.rec[r];
-      const BwdRecord b = p.rec[r + 1];
+      BwdRecord a = p.rec[r];
+      BwdRecord b = p.rec[r + 1];
+      a.t = static_cast<int32_t>(clamp_index(a.t, p.T, p.status));
+      b.t = static_cast<int32_t>(clamp_index(b.t, p.T, p.status));
       const uint4 xa = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(a.t) * D) + c);
       const uint4 xb = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(b.t) * D) + c);
       const float4* ya = reinterpret_cast<const float4*>(p.dy + static_cast<size_t>(a.t) * D) + 2 * c;
@@ -345,7 +359,8 @@ __global__ void __launch_bounds__(384) dw_kernel(const BwdParams p) {
       for (int e = 0; e < 8; ++e) d[e] = fmaf(b.a, ybv[e], fmaf(a.a, yav[e], d[e]));
     }
     for (; r < r1; ++r) {
-      const BwdRecord a = p.rec[r];
+      BwdRecord a = p.rec[r];
+      a.t = static_cast<int32_t>(clamp_index(a.t, p.T, p.status));
       const uint4 xa = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(a.t) * D) + c);
       const float4* ya = reinterpret_cast<const float4*>(p.dy + static_cast<size_t>(a.t) * D) + 2 * c;
       const float4 ya0 = __ldg(ya), ya1 = __ldg(ya + 1);
@@ -537,6 +552,7 @@ twell_status dense_rows_bwd(const uint16_t* x, const hybrid_t* h, const float* U
     g.src = dy;
     g.lds = D;
     g.row_idx = h->dense_rows;
+    g.row_limit = h->T;
     g.R = MD;
     g.C = D;
     g.R_dyn = h->n_dense;
@@ -601,11 +617,12 @@ twell_status dense_rows_bwd(const uint16_t* x, const hybrid_t* h, const float* U
     a.C = dx;
     a.ldc = D;
     a.row_idx = h->dense_rows;
+    a.row_limit = h->T;
     a.status = status_dev;
     a.ksplit = gemm_ksplit(static_cast<int64_t>(num_m) * ((D + (wide ? 255 : 127)) /
                                                            (wide ? 256 : 128)),
                            4 * F64, dev);
-    if ((st = zero_rows(dx, D, h->dense_rows, MD, h->n_dense, D, s)) != TWELL_OK) return st;
+    if ((st = zero_rows(dx, D, h->dense_rows, MD, h->n_dense, D, s, h->T, status_dev)) != TWELL_OK) return st;
     if ((st = gemm_run(maps, a, wide, dev, s)) != TWELL_OK) return st;
   }
   {  // transposed operands of the weight gradients ([F or D][mpad], zero padded)
@@ -617,6 +634,8 @@ twell_status dense_rows_bwd(const uint16_t* x, const hybrid_t* h, const float* U
     tr.src = x;
     tr.lds = D;
     tr.row_idx = h->dense_rows;
+    tr.row_limit = h->T;
+    tr.status = status_dev;
     tr.C = D;
     tr.out_hi = XoT;
     if ((st = transpose_run(0, tr, s)) != TWELL_OK) return st;

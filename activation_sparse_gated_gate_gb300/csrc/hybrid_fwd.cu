@@ -39,6 +39,7 @@ twell_status dense_rows_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t
   g.src = x;
   g.lds = D;
   g.row_idx = h->dense_rows;
+  g.row_limit = h->T;
   g.R = MD;
   g.C = D;
   g.R_dyn = h->n_dense;
@@ -99,11 +100,12 @@ twell_status dense_rows_fwd(const uint16_t* x, const hybrid_t* h, const uint16_t
     a.C = y;
     a.ldc = D;
     a.row_idx = h->dense_rows;
+    a.row_limit = h->T;
     a.status = status_dev;
     a.ksplit = gemm_ksplit(static_cast<int64_t>(num_m) * ((D + (wide ? 255 : 127)) /
                                                            (wide ? 256 : 128)),
                            2 * static_cast<int64_t>(F), dev);
-    if ((st = zero_rows(y, D, h->dense_rows, MD, h->n_dense, D, s)) != TWELL_OK) return st;
+    if ((st = zero_rows(y, D, h->dense_rows, MD, h->n_dense, D, s, h->T, status_dev)) != TWELL_OK) return st;
     if ((st = gemm_run(maps, a, wide, dev, s)) != TWELL_OK) return st;
   }
   return TWELL_OK;

@@ -59,6 +59,7 @@ twell_status gather_rows(int mode, const void* src, const hybrid_t* h, int32_t D
   g.src = src;
   g.lds = D;
   g.row_idx = h->ell_rows;
+  g.row_limit = h->T;
   g.R = h->T;
   g.C = D;
   g.R_dyn = h->n_ell;
@@ -136,6 +137,7 @@ extern "C" twell_status hybrid_ffn_fwd_tc(const uint16_t* x, const hybrid_t* h,
     a.out = y;
     a.ldo = D;
     a.row_idx = h->ell_rows;
+    a.row_limit = h->T;
     if ((st = tc_run(m, a, dev, s)) != TWELL_OK) return st;
   }
   if (h->max_dense == 0) return TWELL_OK;
@@ -233,6 +235,7 @@ extern "C" twell_status hybrid_ffn_bwd_tc(const uint16_t* x, const hybrid_t* h,
     a.out = dx;
     a.ldo = D;
     a.row_idx = h->ell_rows;
+    a.row_limit = h->T;
     if ((st = tc_run(m, a, dev, s)) != TWELL_OK) return st;
   }
   {  // weight gradients of the ELL rows (overwrite)

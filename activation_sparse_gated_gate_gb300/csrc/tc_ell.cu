@@ -34,6 +34,7 @@
 
 #include "ptx.cuh"
 #include "scale.cuh"
+#include "bounds.cuh"
 #include "tc_ell.cuh"
 
 namespace twell {
@@ -510,6 +511,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
           const int i = m_blk * BM + r;
           valid = i < U.n_rows;
           orow = valid ? p.row_idx[i] : 0;
+          if (valid && p.row_limit && !in_bounds(orow, p.row_limit, p.status)) {
+            valid = false;
+            orow = 0;
+          }
         } else {
           orow = m_blk * BM + r;
         }

@@ -73,6 +73,7 @@ struct TcArgs {
   float* out;
   int64_t ldo;
   const int32_t* row_idx;  // ROWS: output row of ELL row i
+  int32_t row_limit;       // rows of out that row_idx may name (0: unchecked)
   int32_t* status;
 };
 

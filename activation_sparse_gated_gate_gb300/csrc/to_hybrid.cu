@@ -15,6 +15,7 @@
 //             slice when W < count <= C)
 //   dense_fill one CTA per dense row: thread j writes ReLU(z) of column j
 //             from the slots or the spill slice (coalesced row writes)
+#include "bounds.cuh"
 #include "common.cuh"
 
 namespace twell {
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
   const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (i >= *p.n_ell) return;
   const int t = p.ell_rows[i];
+  if (!in_bounds(t, p.T, p.status)) return;  // warp-uniform
   const size_t src_rt = static_cast<size_t>(t) * p.n_t;
   const size_t dst_rt = static_cast<size_t>(i) * p.n_t;
   for (int k = lane; k < p.n_t; k += 32) {
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(256) dense_fill_kernel(const HybParams p) {
   const int n = min(*p.n_dense, p.max_dense);
   if (i >= n) return;
   const int t = p.dense_rows[i];
+  if (!in_bounds(t, p.T, p.status)) return;  // CTA-uniform
   const size_t rt0 = static_cast<size_t>(t) * p.n_t;
   float* out = p.dense_h + static_cast<size_t>(i) * p.F;
   for (int j = threadIdx.x; j < p.F; j += blockDim.x) {
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(256) dense_fill_kernel(const HybParams p) {
     } else {
       const uint8_t* sc = p.col + (rt0 + k) * p.W;
       const float* sv = p.val + (rt0 + k) * p.W;
-      for (int s = 0; s < c; ++s)
+      for (int s = 0; s < min(c, p.W); ++s)
         if (sc[s] == cc) v = sv[s];
     }
     out[j] = v;

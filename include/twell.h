@@ -63,7 +63,9 @@ enum {
   TWELL_FLAG_SPILL_FULL = 1,  /* more (row, tile) slices overflowed W than spill_cap */
   TWELL_FLAG_DENSE_FULL = 2,  /* more overflow rows than the hybrid's max_dense */
   TWELL_FLAG_TIMEOUT = 4,     /* a pipeline wait exceeded its bound (about 1 s by default) */
-  TWELL_FLAG_RANGE = 8        /* a value exceeded the fp16 range of an fp16 operand */
+  TWELL_FLAG_RANGE = 8,       /* a value exceeded the fp16 range of an fp16 operand */
+  TWELL_FLAG_BOUNDS = 16      /* bounds-checking build only: a gathered or scattered
+                                 index fell outside its buffer (access skipped) */
 };
 
 #define TWELL_TILE 128
@@ -120,7 +122,7 @@ typedef struct {
  *   x        [T][D] bf16            Wg_t  [F][D] bf16 (= W_g^T)
  *   out      TwELL with out->T == T, out->F == F; the kernel resets
  *            *out->spill_n to 0 first (stream-ordered) and, when
- *            out->block_bits is not NULL, fills it (zeroed first)
+ *            out->block_bits is not NULL, fills every word of it
  *   z_debug  optional [T][F] fp32 copy of z (NULL to skip), for checking
  *   status_dev  device int32, see TWELL_FLAG_*
  * T may be 0 (nothing enqueued).
