@@ -36,7 +36,8 @@ def _inference(w, d, spill_cap=None):
     z = torch.empty((w.T, w.F), dtype=torch.float32, device="cuda")
     tw.twell_gate_pack(d["x"], d["Wg_t"], h, z_debug=z)
     y = tw.twell_ffn_fwd(d["x"], h, d["Wu_t"], d["Wd"])
-    y_tc = tw.twell_ffn_fwd_tc(d["x"], h, d["Wu_t"], d["Wd"])
+    # the tensor-core forward takes d_model in multiples of 64
+    y_tc = tw.twell_ffn_fwd_tc(d["x"], h, d["Wu_t"], d["Wd"]) if w.D % 64 == 0 else y
     torch.cuda.synchronize()
     return h, z, y, y_tc
 
