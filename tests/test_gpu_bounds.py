@@ -69,6 +69,10 @@ def test_inference_under_bounds_checks(T, D, F, p, W, cap):
     for a, b in zip(_slots(h1), _slots(h0)):
         torch.testing.assert_close(a, b, rtol=0, atol=0)
     torch.testing.assert_close(h1.block_bits, h0.block_bits, rtol=0, atol=0)
+    if s0 != 0:
+        # a full spill list: which slices got a slot depends on the order of
+        # atomics, and the rows without one are undefined, so y is not compared
+        return
     # few-row calls split rows over warps and add partial sums with atomics
     torch.testing.assert_close(y1, y0, rtol=1e-5, atol=1e-6)
     if w.D % 64 == 0:
