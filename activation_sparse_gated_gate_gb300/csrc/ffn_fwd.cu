@@ -137,11 +137,18 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
     const int k_end = min(k_begin + p.G, p.n_t);
     uint32_t xb[NC][4];
     float acc[NC][8];
-    bool have_x = false;
     bool any = false;
     const uint16_t* xr = p.x + static_cast<size_t>(t) * D;
+    // x_t is loaded at once, with the counts and slots below in flight, not
+    // after them (at decode sizes every dependent load is a DRAM round trip)
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
+      const uint4 v = own(i) ? __ldg(reinterpret_cast<const uint4*>(xr + 8 * (lane + 32 * i)))
+                             : make_uint4(0, 0, 0, 0);
+      xb[i][0] = v.x;
+      xb[i][1] = v.y;
+      xb[i][2] = v.z;
+      xb[i][3] = v.w;
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
     }
@@ -150,6 +157,13 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
     for (int kb = k_begin; kb < k_end; kb += 32) {
       const int k = kb + lane;
       int c = k < k_end ? p.cnt[row_rt + k] : 0;
+      // the tile's first four slots, loaded beside its count (used below
+      // when the count is known; read past the count, never used there)
+      const bool pre = (p.W & 3) == 0 && k < k_end;
+      const size_t so_k = (row_rt + k) * static_cast<size_t>(p.W);
+      const float4 v_pre =
+          pre ? __ldg(reinterpret_cast<const float4*>(p.val + so_k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t c_pre = pre ? __ldg(reinterpret_cast<const uint32_t*>(p.col + so_k)) : 0u;
       if (!in_bounds(c, (ELL ? p.W : TWELL_TILE) + 1, p.status)) c = 0;
       // entries of tile k: its slots, or the positives of its spill slice
       // (the spill holds exactly c positive values)
@@ -170,19 +184,7 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
       }
       const int total = __shfl_sync(0xffffffffu, off, 31);
       off -= n;
-      if (total > 0 && !have_x) {
-        have_x = true;
-        any = true;
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          uint4 v = own(i) ? __ldg(reinterpret_cast<const uint4*>(xr + 8 * (lane + 32 * i)))
-                           : make_uint4(0, 0, 0, 0);
-          xb[i][0] = v.x;
-          xb[i][1] = v.y;
-          xb[i][2] = v.z;
-          xb[i][3] = v.w;
-        }
-      }
+      any |= total > 0;
 
       for (int base = 0; base < total; base += kListCap) {
         // list the entries whose position falls in [base, base + kListCap)
@@ -195,8 +197,10 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
             if ((p.W & 3) == 0) {
               // four slots per 16-byte load (slots past the count are read, not used)
               for (int q = s0 & ~3; q < s1; q += 4) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(p.val + so + q));
-                const uint32_t c4 = __ldg(reinterpret_cast<const uint32_t*>(p.col + so + q));
+                const float4 v =
+                    q == 0 ? v_pre : __ldg(reinterpret_cast<const float4*>(p.val + so + q));
+                const uint32_t c4 =
+                    q == 0 ? c_pre : __ldg(reinterpret_cast<const uint32_t*>(p.col + so + q));
                 const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {

@@ -305,14 +305,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nb = min(DM, p.N - tb);
         bool any = false;
         for (int c = tb; c < tb + nb; c += 16) {
+          // the partner's 16 partial sums first (one round trip for all),
+          // then this CTA's from TMEM
+          float pv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pv[j] = ptx::ld_cluster_f32(part1 + static_cast<uint32_t>((c + j) * kRowBytes + n * 4));
           uint32_t r[16];
           ptx::tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(c), r);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int t = c + j;
-            const float v = __uint_as_float(r[j]) +
-                            ptx::ld_cluster_f32(part1 + static_cast<uint32_t>(t * kRowBytes + n * 4));
+            const float v = __uint_as_float(r[j]) + pv[j];
             *reinterpret_cast<float*>(zt + zoff(t - tb, n)) = v;
             any |= t < p.T && v > 0.0f;
           }

@@ -365,9 +365,11 @@ __device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
   return r;
 }
 
+// (No memory clobber: a run of these loads issues back to back; order them
+// after the writer with cluster_sync, which has one.)
 __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
   return v;
 }
 
