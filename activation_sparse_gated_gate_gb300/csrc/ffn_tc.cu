@@ -18,12 +18,26 @@
 // The union's weight rows are gathered into the 128-byte-swizzled operand
 // tiles by four warps with 16-byte cp.async copies (each copy lands where a
 // TMA box with that swizzle would put it); the token tiles (x, a) come by
-// TMA.  The union bitmap of each block comes from the gate kernel (TwELL
-// block_bits) or, without it, from a small kernel over the TwELL; a scan
-// kernel turns it into U (padded with neuron 0 to a multiple of 256), the
-// per-word position prefix and the list of (block, 256-position chunk) units
-// of the up GEMM.  The up epilogue finds its row's entries in the chunk from
-// the TwELL itself while the chunk's MMAs run.
+// TMA.
+//
+// Token blocks are formed by activity, not by position: the work of a block
+// is set by its union, and the union of 128 tokens grows with their summed
+// activity in a concave way (1 - prod(1 - p_t) per neuron), so blocks of
+// tokens with similar counts of active neurons have a smaller total union
+// than blocks of consecutive tokens wherever the per-token activity varies
+// (a heavy-tailed batch: 55 % of d_ff per block instead of 73 % in the
+// 1.5B-class workload).  Three small kernels sort the tokens, stably, by a
+// logarithmic bucket of their active count (eight buckets per octave) into a
+// permutation; a fourth copies x into that order for the up GEMM's TMA
+// tiles, the down epilogue writes each y row to its token, and the rest of
+// the pipeline works on token positions.
+//
+// The union bitmap of each block of positions comes from a small kernel over
+// the TwELL entries of its tokens; a scan kernel turns it into U (padded
+// with neuron 0 to a multiple of 256), the per-word position prefix and the
+// list of (block, 256-position chunk) units of the up GEMM.  The up epilogue
+// finds its row's entries in the chunk from the TwELL itself while the
+// chunk's MMAs run.
 //
 // Both GEMMs: one persistent CTA per SM, tiles of 128 x 256 outputs, K in
 // blocks of 64, four shared-memory stages [A 16 KB][B 32 KB]:
@@ -98,12 +112,22 @@ struct UgArgs {
   int32_t* units;   // [n_m * nj] up-GEMM units (block * nj + chunk)
   int32_t* wpre;    // [n_m][nw] union position of each bitmap word's first bit
   uint16_t* abuf;   // [T][Fp] a = fp16(h u) in union-position order
+  // token order: position i holds token perm[i]
+  int32_t* perm;    // [T]
+  uint8_t* keys;    // [T] activity bucket of each token
+  int32_t* hist;    // [n_sort][UG_NBUCKET] bucket counts, then start positions
+  int32_t n_sort;   // sort CTAs (UG_SORT_THREADS tokens each)
+  const uint16_t* x;  // [T][D] bf16, token order
+  uint16_t* xp;       // [T][D] bf16, position order (the up GEMM's A)
   int32_t* status;
 };
 
+constexpr int UG_SORT_THREADS = 1024;  // tokens per sort CTA
+constexpr int UG_NBUCKET = 128;        // activity buckets (eight per octave)
+
 struct UgLayout {
-  size_t ctr, gbm, nU, Ulist, units, wpre, abuf, wd16, bytes;
-  int64_t Fp, nw, n_m, nj;
+  size_t ctr, gbm, nU, Ulist, units, wpre, abuf, wd16, perm, keys, hist, xp, bytes;
+  int64_t Fp, nw, n_m, nj, n_sort;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -131,15 +155,27 @@ UgLayout ug_layout(int64_t T, int64_t D, int64_t F) {
   o = up256(o + static_cast<size_t>(T) * L.Fp * 2);
   L.wd16 = o;
   o = up256(o + static_cast<size_t>(F) * D * 2);
+  L.n_sort = (T + UG_SORT_THREADS - 1) / UG_SORT_THREADS;
+  L.perm = o;
+  o = up256(o + static_cast<size_t>(T) * 4);
+  L.keys = o;
+  o = up256(o + static_cast<size_t>(T));
+  L.hist = o;
+  o = up256(o + static_cast<size_t>(L.n_sort) * UG_NBUCKET * 4);
+  L.xp = o;
+  o = up256(o + static_cast<size_t>(T) * D * 2);
   L.bytes = o;
   return L;
 }
 
 // ------------------------------------------------------------ preparation
-//   ug_bits_kernel  (only for a TwELL without block_bits; grid: blocks x 8
-//                   CTAs of 16 rows) ORs every active neuron of its rows
-//                   into the block's union bitmap (shared memory, then global
-//                   atomics into the zeroed [n_m][nw] bitmap).
+//   ug_key_kernel, ug_hist_scan_kernel, ug_place_kernel  sort the tokens
+//                   into positions (see the header); ug_perm_x_kernel copies
+//                   x into position order.
+//   ug_bits_kernel  (grid: blocks x 8 CTAs of 16 positions) ORs every active
+//                   neuron of its positions' tokens into the block's union
+//                   bitmap (shared memory, then global atomics into the
+//                   zeroed [n_m][nw] bitmap).
 //   ug_scan_kernel  (one CTA per block) takes the exclusive prefix of the
 //                   bitmap words' popcounts -- a neuron's union position is
 //                   the prefix of its word plus the set bits below it in the
@@ -173,6 +209,109 @@ __device__ __forceinline__ void ug_walk_pair(const UgArgs& p, size_t rt, int k, 
   }
 }
 
+// Activity bucket of a token with n active neurons: eight buckets per octave
+// of n + 1 (n + 1 < 8 exactly), monotone in n.
+__device__ __forceinline__ int ug_bucket(int n) {
+  const int v = n + 1;
+  const int e = 31 - __clz(v);
+  const int b = e < 3 ? v : 8 * (e - 2) + ((v >> (e - 3)) & 7);
+  return min(b, UG_NBUCKET - 1);
+}
+
+// One thread per token: its bucket (from the TwELL counts of its row) into
+// keys[t], and the CTA's bucket counts into hist[cta][*].
+__global__ void __launch_bounds__(UG_SORT_THREADS) ug_key_kernel(const UgArgs p) {
+  __shared__ int h[UG_NBUCKET];
+  for (int i = threadIdx.x; i < UG_NBUCKET; i += UG_SORT_THREADS) h[i] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * UG_SORT_THREADS + threadIdx.x;
+  if (t < p.T) {
+    const uint8_t* row = p.cnt + static_cast<size_t>(t) * p.n_t;
+    int n = 0;
+    if ((p.n_t & 3) == 0) {
+      for (int k = 0; k < p.n_t; k += 4) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(row + k));
+        const uint32_t s2 = (w & 0x00ff00ffu) + ((w >> 8) & 0x00ff00ffu);
+        n += static_cast<int>((s2 & 0xffffu) + (s2 >> 16));
+      }
+    } else {
+      for (int k = 0; k < p.n_t; ++k) n += row[k];
+    }
+    const int b = ug_bucket(n);
+    p.keys[t] = static_cast<uint8_t>(b);
+    atomicAdd(&h[b], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < UG_NBUCKET; i += UG_SORT_THREADS)
+    p.hist[static_cast<size_t>(blockIdx.x) * UG_NBUCKET + i] = h[i];
+}
+
+// One CTA: hist[c][b] becomes the first position of bucket b's tokens of
+// sort CTA c (buckets in order, CTAs in order within a bucket).
+__global__ void __launch_bounds__(UG_NBUCKET) ug_hist_scan_kernel(const UgArgs p) {
+  __shared__ int tot[UG_NBUCKET];
+  const int b = threadIdx.x;
+  int sum = 0;
+  for (int c = 0; c < p.n_sort; ++c) sum += p.hist[static_cast<size_t>(c) * UG_NBUCKET + b];
+  tot[b] = sum;
+  __syncthreads();
+  int start = 0;
+  for (int i = 0; i < b; ++i) start += tot[i];
+  for (int c = 0; c < p.n_sort; ++c) {
+    int* hp = p.hist + static_cast<size_t>(c) * UG_NBUCKET + b;
+    const int v = *hp;
+    *hp = start;
+    start += v;
+  }
+}
+
+// One thread per token: its position = the start of its bucket in its sort
+// CTA + the tokens of the same bucket before it in the CTA (warp match and
+// per-warp counts), so the order is stable.
+__global__ void __launch_bounds__(UG_SORT_THREADS) ug_place_kernel(const UgArgs p) {
+  constexpr int kWarps = UG_SORT_THREADS / 32;
+  __shared__ int wc[kWarps][UG_NBUCKET];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kWarps * UG_NBUCKET; i += UG_SORT_THREADS)
+    wc[i / UG_NBUCKET][i % UG_NBUCKET] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * UG_SORT_THREADS + threadIdx.x;
+  const bool valid = t < p.T;
+  const int b = valid ? p.keys[t] : UG_NBUCKET;  // an out-of-range key for the tail
+  const uint32_t same = __match_any_sync(0xffffffffu, b);
+  const int rank = __popc(same & ((1u << lane) - 1u));
+  if (valid && rank == 0) wc[warp][b] = __popc(same);
+  __syncthreads();
+  // exclusive prefix over the warps, per bucket
+  for (int i = threadIdx.x; i < UG_NBUCKET; i += UG_SORT_THREADS) {
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = wc[w][i];
+      wc[w][i] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    const int pos = p.hist[static_cast<size_t>(blockIdx.x) * UG_NBUCKET + b] + wc[warp][b] + rank;
+    if (in_bounds(pos, p.T, p.status)) p.perm[pos] = t;
+  }
+}
+
+// xp[i] = x[perm[i]] (rows of D bf16, 16 bytes per step).
+__global__ void __launch_bounds__(256) ug_perm_x_kernel(const UgArgs p) {
+  const int per_row = p.D / 8;
+  const long long total = static_cast<long long>(p.T) * per_row;
+  for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(v / per_row);
+    const int q = static_cast<int>(v % per_row);
+    const int t = static_cast<int>(clamp_index(p.perm[i], p.T, p.status));
+    reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(i) * p.D)[q] =
+        __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.D) + q);
+  }
+}
+
 __global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p) {
   extern __shared__ uint32_t psm[];
   const int nw = p.nw;
@@ -184,10 +323,12 @@ __global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p
   for (int i = threadIdx.x; i < nw; i += UG_PREP_THREADS) bm[i] = 0u;
   __syncthreads();
   const int n_t = p.n_t;
-  const size_t rt0 = static_cast<size_t>(r0) * n_t;  // the rows' (row, tile) pairs are contiguous
-  for (int q = threadIdx.x; q < rows * n_t; q += UG_PREP_THREADS)
-    ug_walk_pair(p, rt0 + q, q % n_t, true,
+  for (int q = threadIdx.x; q < rows * n_t; q += UG_PREP_THREADS) {
+    const int tok = p.perm[r0 + q / n_t];
+    if (!in_bounds(tok, p.T, p.status)) continue;
+    ug_walk_pair(p, static_cast<size_t>(tok) * n_t + q % n_t, q % n_t, true,
                  [&](int n, float) { atomicOr(&bm[n >> 5], 1u << (n & 31)); });
+  }
   __syncthreads();
   uint32_t* g = p.gbm + static_cast<size_t>(m) * p.gbm_pitch;
   for (int i = threadIdx.x; i < nw; i += UG_PREP_THREADS)
@@ -621,8 +762,9 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       const UgUnit U = Un;
       if (u + static_cast<int>(gridDim.x) < num_units)
         Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
-      const int t = U.m * UG_BM + r;
-      const bool valid = t < p.T;
+      const int pos = U.m * UG_BM + r;  // position of this row
+      const bool valid = pos < p.T;
+      const int t = valid ? static_cast<int>(clamp_index(p.perm[pos], p.T, p.status)) : 0;
       if (MODE == UG_DOWN && U.kb == 0) {  // no active neuron in the block: y rows are zero
         if (valid) {
           float* o = p.y + static_cast<size_t>(t) * p.D + U.n0 + 128 * set;
@@ -734,11 +876,17 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
             }
           }
         } else {
-          // 128-byte rows, 128-byte swizzle: chunk j of row lane at j ^ (lane & 7)
+          // y rows go to their tokens: each thread stores its row's 32
+          // values (128 contiguous bytes) directly
+          if (valid) {
+            float4* o = reinterpret_cast<float4*>(p.y + static_cast<size_t>(t) * p.D + U.n0 +
+                                                  128 * set + 32 * c);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+              o[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+          continue;
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -847,15 +995,21 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   a.Wd = Wd;
   a.y = y;
   a.ctr = reinterpret_cast<int32_t*>(w + L.ctr);
-  // the gate kernel's block bitmaps when the TwELL has them, else our own
-  const bool own_bits = h->block_bits == nullptr;
-  a.gbm = own_bits ? reinterpret_cast<uint32_t*>(w + L.gbm) : h->block_bits;
-  a.gbm_pitch = own_bits ? static_cast<int32_t>(L.nw) : F / 32;
+  // block bitmaps of the sorted blocks of positions (the gate kernel's
+  // bitmaps describe blocks of consecutive tokens and are not used)
+  a.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
+  a.gbm_pitch = static_cast<int32_t>(L.nw);
   a.nU = reinterpret_cast<int32_t*>(w + L.nU);
   a.Ulist = reinterpret_cast<int32_t*>(w + L.Ulist);
   a.units = reinterpret_cast<int32_t*>(w + L.units);
   a.wpre = reinterpret_cast<int32_t*>(w + L.wpre);
   a.abuf = reinterpret_cast<uint16_t*>(w + L.abuf);
+  a.perm = reinterpret_cast<int32_t*>(w + L.perm);
+  a.keys = w + L.keys;
+  a.hist = reinterpret_cast<int32_t*>(w + L.hist);
+  a.n_sort = static_cast<int32_t>(L.n_sort);
+  a.x = x;
+  a.xp = reinterpret_cast<uint16_t*>(w + L.xp);
   // the caller's fp16 copy of W_d, or one made in the workspace below
   a.Wd16 = Wd_f16 ? const_cast<uint16_t*>(Wd_f16) : reinterpret_cast<uint16_t*>(w + L.wd16);
   a.status = status_dev;
@@ -863,7 +1017,7 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   // operand maps (box 64 x 128, 128-byte swizzle) and output maps (box
   // 32 x 32: a in bf16 with the 64-byte swizzle, y in fp32 with 128)
   CUtensorMap map_x, map_a, map_as, map_y;
-  if ((st = tc_map_a(&map_x, x, T, D, 0)) != TWELL_OK) return st;
+  if ((st = tc_map_a(&map_x, a.xp, T, D, 0)) != TWELL_OK) return st;
   if ((st = tc_map_a(&map_a, a.abuf, T, L.Fp, 0)) != TWELL_OK) return st;
   if ((st = make_tmap_2d(&map_as, 2, a.abuf, L.Fp, T, 32, 32, L.Fp * 2, 64)) != TWELL_OK)
     return st;
@@ -871,14 +1025,21 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
       TWELL_OK)
     return st;
 
-  // the counter and our block bitmaps are adjacent: one memset clears both
-  if (cudaMemsetAsync(w + L.ctr, 0, own_bits ? L.nU - L.ctr : 256, s) != cudaSuccess)
-    return TWELL_ERR_CUDA;
-  const dim3 pgrid(a.n_m, UG_BM / UG_ROWS_PER_CTA);
-  if (own_bits) {
-    ug_bits_kernel<<<pgrid, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 4, s>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  // the counter and the block bitmaps are adjacent: one memset clears both
+  if (cudaMemsetAsync(w + L.ctr, 0, L.nU - L.ctr, s) != cudaSuccess) return TWELL_ERR_CUDA;
+  // token order, x in that order, then the blocks' unions
+  ug_key_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
+  ug_hist_scan_kernel<<<1, UG_NBUCKET, 0, s>>>(a);
+  ug_place_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
+  {
+    const long long n16 = static_cast<long long>(T) * (D / 8);
+    const long long want = (n16 + 255) / 256;
+    const long long cap = 8ll * dev.sm_count;
+    ug_perm_x_kernel<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(a);
   }
+  const dim3 pgrid(a.n_m, UG_BM / UG_ROWS_PER_CTA);
+  ug_bits_kernel<<<pgrid, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 4, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
   ug_scan_kernel<<<a.n_m, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 8, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
   if (!Wd_f16) {

@@ -164,9 +164,12 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
 /*
  * Tensor-core variant of twell_ffn_fwd (paper section 2.B.2: up and down
  * projections of the active neurons only, built to keep the tensor cores
- * busy).  Same function, different arithmetic: for each block of 128 rows
- * the union U of the rows' active neurons (h->block_bits when it is not
- * NULL, else built from the slots and spill slices) is gathered, u = x W_u[:, U] is
+ * busy).  Same function, different arithmetic: the rows are first ordered by
+ * their count of active neurons (a stable sort into eight buckets per octave;
+ * blocks of rows with similar activity have smaller unions), then for each
+ * block of 128 rows in that order the union U of the rows' active neurons
+ * (built from the slots and spill slices; h->block_bits is not read) is
+ * gathered, u = x W_u[:, U] is
  * one tcgen05 GEMM (bf16 in, fp32 out), a = h u is rounded to fp16 at each
  * row's own active neurons (0 at the union's other positions), and
  * y = a W_d[U, :] is a second tcgen05 GEMM on fp16 operands (W_d converted
@@ -180,9 +183,9 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
  *   Wd_f16  optional [F][D] fp16 copy of Wd (twell_to_f16); NULL: the call
  *           makes one in the workspace (one extra pass over W_d)
  *   ws: twell_workspace_size(TWELL_WS_FFN_FWD_TC, T, D, F, 0, 0) bytes,
- *       256-byte aligned (per-block unions and position prefixes, the
- *       [T][F] fp16 matrix of a in union order and the fp16 copy of W_d:
- *       about 2 (T + D) F bytes)
+ *       256-byte aligned (the row order, x in that order, per-block unions
+ *       and position prefixes, the [T][F] fp16 matrix of a in union order
+ *       and the fp16 copy of W_d: about 2 (T + D) F + 2 T D bytes)
  * A (row, tile) whose spill slice is missing is skipped and
  * TWELL_FLAG_SPILL_FULL is set.  Results do not depend on how the work is
  * scheduled: repeated calls agree bit for bit.  T may be 0.
