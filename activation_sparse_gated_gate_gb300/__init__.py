@@ -19,13 +19,14 @@ import torch
 
 __all__ = [
     "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
-    "twell_ffn_fwd_tc", "twell_to_f16",
+    "twell_ffn_fwd_tc", "twell_ffn_fwd_tc_sorted", "twell_to_f16",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd", "hybrid_ffn_fwd_tc", "hybrid_ffn_bwd_tc",
     "twell_status_string", "twell_probe_fma", "twell_gate_pack_wait_limit",
     "FLAG_SPILL_FULL", "FLAG_DENSE_FULL", "FLAG_TIMEOUT", "FLAG_RANGE", "FLAG_BOUNDS", "TILE",
     "library",
     "WS_HYBRID_FWD", "WS_HYBRID_BWD", "WS_HYBRID_FWD_TC", "WS_HYBRID_BWD_TC", "WS_FFN_FWD_TC",
+    "WS_FFN_FWD_TC_SORTED",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -78,6 +79,8 @@ _SIGNATURES = {
                               c_ptr, c_ptr]),
     "twell_ffn_fwd_tc": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_ptr, c_i32,
                                  c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "twell_ffn_fwd_tc_sorted": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_ptr,
+                                        c_i32, c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "twell_to_f16": (c_i32, [c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "twell_to_hybrid": (c_i32, [ctypes.POINTER(TwellStruct), ctypes.POINTER(HybridStruct),
                                 c_ptr, c_ptr]),
@@ -266,12 +269,14 @@ def twell_to_f16(src, dst=None, status=None, stream=None):
 
 
 def twell_ffn_fwd_tc(x, h: TwELL, Wu_t, Wd, y=None, ws=None, Wd_f16=None, status=None,
-                     stream=None):
+                     stream=None, sorted_rows=False):
     """Tensor-core (union-gather) up + down projection from the TwELL gate
     ``h``: the same function as ``twell_ffn_fwd`` with h*u rounded to fp16;
     returns y [T][D] fp32 (allocated if not given).  ``ws`` is the device
     workspace (allocated if not given); ``Wd_f16`` an optional fp16 copy of
-    ``Wd`` (``twell_to_f16``), made by the call when not given."""
+    ``Wd`` (``twell_to_f16``), made by the call when not given.  With
+    ``sorted_rows`` the call is ``twell_ffn_fwd_tc_sorted`` (token blocks
+    grouped by activity)."""
     _need(x, torch.bfloat16, "x")
     _need(Wu_t, torch.bfloat16, "Wu_t")
     _need(Wd, torch.bfloat16, "Wd")
@@ -284,17 +289,28 @@ def twell_ffn_fwd_tc(x, h: TwELL, Wu_t, Wd, y=None, ws=None, Wd_f16=None, status
     if Wd_f16 is not None and (Wd_f16.dtype != torch.float16 or Wd_f16.shape != Wd.shape
                                or not Wd_f16.is_contiguous()):
         raise ValueError("Wd_f16 must be a contiguous fp16 copy of Wd")
-    nbytes = twell_workspace_size(WS_FFN_FWD_TC, T, D, h.F, 0, 0)
+    op = WS_FFN_FWD_TC_SORTED if sorted_rows else WS_FFN_FWD_TC
+    name = "twell_ffn_fwd_tc_sorted" if sorted_rows else "twell_ffn_fwd_tc"
+    nbytes = twell_workspace_size(op, T, D, h.F, 0, 0)
     if ws is None:
         ws = _workspace(nbytes, x.device)
     status = h.status if status is None else status
     with torch.cuda.device(x.device):
-        _check(lib().twell_ffn_fwd_tc(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd),
-                                      _ptr(Wd_f16), D, _ptr(y), _ptr(ws),
-                                      ws.numel() * ws.element_size(), _ptr(status),
-                                      _stream(stream)),
-               "twell_ffn_fwd_tc")
+        _check(getattr(lib(), name)(_ptr(x), ctypes.byref(h.struct), _ptr(Wu_t), _ptr(Wd),
+                                    _ptr(Wd_f16), D, _ptr(y), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _ptr(status),
+                                    _stream(stream)),
+               name)
     return y
+
+
+def twell_ffn_fwd_tc_sorted(x, h: TwELL, Wu_t, Wd, y=None, ws=None, Wd_f16=None, status=None,
+                            stream=None):
+    """``twell_ffn_fwd_tc`` on token blocks grouped by activity (rows sorted
+    by their count of active neurons); same result, less GEMM work when the
+    per-token activity varies widely."""
+    return twell_ffn_fwd_tc(x, h, Wu_t, Wd, y=y, ws=ws, Wd_f16=Wd_f16, status=status,
+                            stream=stream, sorted_rows=True)
 
 
 class Hybrid:
@@ -349,6 +365,7 @@ WS_HYBRID_BWD = 2
 WS_HYBRID_FWD_TC = 3
 WS_HYBRID_BWD_TC = 4
 WS_FFN_FWD_TC = 5
+WS_FFN_FWD_TC_SORTED = 6
 
 
 def twell_workspace_size(op: int, T: int, D: int, F: int, cap: int, max_dense: int) -> int:

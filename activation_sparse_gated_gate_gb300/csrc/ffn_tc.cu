@@ -20,7 +20,8 @@
 // TMA box with that swizzle would put it); the token tiles (x, a) come by
 // TMA.
 //
-// Token blocks are formed by activity, not by position: the work of a block
+// Optionally (twell_ffn_fwd_tc_sorted) token blocks are formed by activity,
+// not by position: the work of a block
 // is set by its union, and the union of 128 tokens grows with their summed
 // activity in a concave way (1 - prod(1 - p_t) per neuron), so blocks of
 // tokens with similar counts of active neurons have a smaller total union
@@ -30,9 +31,12 @@
 // logarithmic bucket of their active count (eight buckets per octave) into a
 // permutation; a fourth copies x into that order for the up GEMM's TMA
 // tiles, the down epilogue writes each y row to its token, and the rest of
-// the pipeline works on token positions.
+// the pipeline works on token positions.  In a batch whose tokens are about
+// equally active the sort gains nothing and costs its kernels, so the plain
+// entry point keeps blocks of consecutive tokens.
 //
-// The union bitmap of each block of positions comes from a small kernel over
+// The union bitmap of each block comes from the gate kernel (TwELL
+// block_bits, blocks of consecutive tokens only) or from a small kernel over
 // the TwELL entries of its tokens; a scan kernel turns it into U (padded
 // with neuron 0 to a multiple of 256), the per-word position prefix and the
 // list of (block, 256-position chunk) units of the up GEMM.  The up epilogue
@@ -112,7 +116,8 @@ struct UgArgs {
   int32_t* units;   // [n_m * nj] up-GEMM units (block * nj + chunk)
   int32_t* wpre;    // [n_m][nw] union position of each bitmap word's first bit
   uint16_t* abuf;   // [T][Fp] a = fp16(h u) in union-position order
-  // token order: position i holds token perm[i]
+  // token order (sorted variant): position i holds token perm[i]; NULL:
+  // position i is token i
   int32_t* perm;    // [T]
   uint8_t* keys;    // [T] activity bucket of each token
   int32_t* hist;    // [n_sort][UG_NBUCKET] bucket counts, then start positions
@@ -132,7 +137,7 @@ struct UgLayout {
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-UgLayout ug_layout(int64_t T, int64_t D, int64_t F) {
+UgLayout ug_layout(int64_t T, int64_t D, int64_t F, bool sorted) {
   UgLayout L{};
   L.Fp = (F + 255) / 256 * 256;
   L.nw = L.Fp / 32;
@@ -156,6 +161,11 @@ UgLayout ug_layout(int64_t T, int64_t D, int64_t F) {
   L.wd16 = o;
   o = up256(o + static_cast<size_t>(F) * D * 2);
   L.n_sort = (T + UG_SORT_THREADS - 1) / UG_SORT_THREADS;
+  if (!sorted) {
+    L.perm = L.keys = L.hist = L.xp = 0;
+    L.bytes = o;
+    return L;
+  }
   L.perm = o;
   o = up256(o + static_cast<size_t>(T) * 4);
   L.keys = o;
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p
   __syncthreads();
   const int n_t = p.n_t;
   for (int q = threadIdx.x; q < rows * n_t; q += UG_PREP_THREADS) {
-    const int tok = p.perm[r0 + q / n_t];
+    const int tok = p.perm ? p.perm[r0 + q / n_t] : r0 + q / n_t;
     if (!in_bounds(tok, p.T, p.status)) continue;
     ug_walk_pair(p, static_cast<size_t>(tok) * n_t + q % n_t, q % n_t, true,
                  [&](int n, float) { atomicOr(&bm[n >> 5], 1u << (n & 31)); });
@@ -764,7 +774,9 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
         Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
       const int pos = U.m * UG_BM + r;  // position of this row
       const bool valid = pos < p.T;
-      const int t = valid ? static_cast<int>(clamp_index(p.perm[pos], p.T, p.status)) : 0;
+      const int t = !valid ? 0
+                    : p.perm ? static_cast<int>(clamp_index(p.perm[pos], p.T, p.status))
+                             : pos;
       if (MODE == UG_DOWN && U.kb == 0) {  // no active neuron in the block: y rows are zero
         if (valid) {
           float* o = p.y + static_cast<size_t>(t) * p.D + U.n0 + 128 * set;
@@ -876,17 +888,32 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
             }
           }
         } else {
-          // y rows go to their tokens: each thread stores its row's 32
-          // values (128 contiguous bytes) directly
-          if (valid) {
-            float4* o = reinterpret_cast<float4*>(p.y + static_cast<size_t>(t) * p.D + U.n0 +
-                                                  128 * set + 32 * c);
+          // 128-byte rows, 128-byte swizzle: chunk j of row lane at j ^ (lane & 7)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              o[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (p.perm) {
+            // rows in sorted order go to their tokens: the staged box is read
+            // back four rows per pass, eight lanes per row (one 16-byte chunk
+            // each), so every store writes four whole 128-byte row segments
+            __syncwarp();
+            const int sub = lane >> 3;   // row within the pass
+            const int ch = lane & 7;     // chunk of the row
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = 4 * i + sub;  // row of the warp's box
+              const int tr = __shfl_sync(0xffffffffu, t, rr);
+              const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
+              const uint4 w = *reinterpret_cast<const uint4*>(buf + rr * 128 +
+                                                              ((ch ^ (rr & 7)) << 4));
+              if (vr)
+                reinterpret_cast<uint4*>(p.y + static_cast<size_t>(tr) * p.D + U.n0 +
+                                         128 * set + 32 * c)[ch] = w;
+            }
+            __syncwarp();  // the buffer is rewritten by the next chunk
+            continue;
           }
-          continue;
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -927,8 +954,8 @@ twell_status ug_launch(const CUtensorMap& map, const CUtensorMap& map_out, const
 
 }  // namespace
 
-size_t ffn_tc_workspace_bytes(int64_t T, int64_t D, int64_t F) {
-  return ug_layout(T, D, F).bytes;
+size_t ffn_tc_workspace_bytes(int64_t T, int64_t D, int64_t F, bool sorted) {
+  return ug_layout(T, D, F, sorted).bytes;
 }
 
 }  // namespace twell
@@ -950,11 +977,13 @@ extern "C" twell_status twell_to_f16(const uint16_t* src, uint16_t* dst, size_t 
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
-extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
-                                         const uint16_t* Wu_t, const uint16_t* Wd,
-                                         const uint16_t* Wd_f16, int32_t D, float* y, void* ws,
-                                         size_t ws_bytes, int32_t* status_dev, void* stream) {
-  using namespace twell;
+namespace twell {
+namespace {
+
+twell_status ffn_tc_run(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
+                        const uint16_t* Wd, const uint16_t* Wd_f16, int32_t D, float* y,
+                        void* ws, size_t ws_bytes, int32_t* status_dev, void* stream,
+                        bool sorted) {
   if (h == nullptr) return TWELL_ERR_INVALID;
   const int32_t T = h->T, F = h->F;
   if (T < 0 || F <= 0 || F % TWELL_TILE != 0 || D <= 0 || D % UG_BK != 0)
@@ -967,7 +996,7 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   if (!aligned16(x) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y) ||
       (Wd_f16 && !aligned16(Wd_f16)) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return TWELL_ERR_INVALID;
-  const UgLayout L = ug_layout(T, D, F);
+  const UgLayout L = ug_layout(T, D, F, sorted);
   if (ws_bytes < L.bytes) return TWELL_ERR_INVALID;
   DeviceInfo dev;
   if ((st = require_sm103(&dev)) != TWELL_OK) return st;
@@ -995,21 +1024,22 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   a.Wd = Wd;
   a.y = y;
   a.ctr = reinterpret_cast<int32_t*>(w + L.ctr);
-  // block bitmaps of the sorted blocks of positions (the gate kernel's
-  // bitmaps describe blocks of consecutive tokens and are not used)
-  a.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
-  a.gbm_pitch = static_cast<int32_t>(L.nw);
+  // the gate kernel's block bitmaps when the TwELL has them and the blocks
+  // are its blocks of consecutive tokens, else our own
+  const bool own_bits = sorted || h->block_bits == nullptr;
+  a.gbm = own_bits ? reinterpret_cast<uint32_t*>(w + L.gbm) : h->block_bits;
+  a.gbm_pitch = own_bits ? static_cast<int32_t>(L.nw) : F / 32;
   a.nU = reinterpret_cast<int32_t*>(w + L.nU);
   a.Ulist = reinterpret_cast<int32_t*>(w + L.Ulist);
   a.units = reinterpret_cast<int32_t*>(w + L.units);
   a.wpre = reinterpret_cast<int32_t*>(w + L.wpre);
   a.abuf = reinterpret_cast<uint16_t*>(w + L.abuf);
-  a.perm = reinterpret_cast<int32_t*>(w + L.perm);
-  a.keys = w + L.keys;
-  a.hist = reinterpret_cast<int32_t*>(w + L.hist);
+  a.perm = sorted ? reinterpret_cast<int32_t*>(w + L.perm) : nullptr;
+  a.keys = sorted ? w + L.keys : nullptr;
+  a.hist = sorted ? reinterpret_cast<int32_t*>(w + L.hist) : nullptr;
   a.n_sort = static_cast<int32_t>(L.n_sort);
   a.x = x;
-  a.xp = reinterpret_cast<uint16_t*>(w + L.xp);
+  a.xp = sorted ? reinterpret_cast<uint16_t*>(w + L.xp) : nullptr;
   // the caller's fp16 copy of W_d, or one made in the workspace below
   a.Wd16 = Wd_f16 ? const_cast<uint16_t*>(Wd_f16) : reinterpret_cast<uint16_t*>(w + L.wd16);
   a.status = status_dev;
@@ -1017,7 +1047,7 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   // operand maps (box 64 x 128, 128-byte swizzle) and output maps (box
   // 32 x 32: a in bf16 with the 64-byte swizzle, y in fp32 with 128)
   CUtensorMap map_x, map_a, map_as, map_y;
-  if ((st = tc_map_a(&map_x, a.xp, T, D, 0)) != TWELL_OK) return st;
+  if ((st = tc_map_a(&map_x, sorted ? a.xp : x, T, D, 0)) != TWELL_OK) return st;
   if ((st = tc_map_a(&map_a, a.abuf, T, L.Fp, 0)) != TWELL_OK) return st;
   if ((st = make_tmap_2d(&map_as, 2, a.abuf, L.Fp, T, 32, 32, L.Fp * 2, 64)) != TWELL_OK)
     return st;
@@ -1025,21 +1055,24 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
       TWELL_OK)
     return st;
 
-  // the counter and the block bitmaps are adjacent: one memset clears both
-  if (cudaMemsetAsync(w + L.ctr, 0, L.nU - L.ctr, s) != cudaSuccess) return TWELL_ERR_CUDA;
-  // token order, x in that order, then the blocks' unions
-  ug_key_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
-  ug_hist_scan_kernel<<<1, UG_NBUCKET, 0, s>>>(a);
-  ug_place_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
-  {
+  // the counter and our block bitmaps are adjacent: one memset clears both
+  if (cudaMemsetAsync(w + L.ctr, 0, own_bits ? L.nU - L.ctr : 256, s) != cudaSuccess)
+    return TWELL_ERR_CUDA;
+  if (sorted) {
+    // token order, then x in that order
+    ug_key_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
+    ug_hist_scan_kernel<<<1, UG_NBUCKET, 0, s>>>(a);
+    ug_place_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
     const long long n16 = static_cast<long long>(T) * (D / 8);
     const long long want = (n16 + 255) / 256;
     const long long cap = 8ll * dev.sm_count;
     ug_perm_x_kernel<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(a);
   }
   const dim3 pgrid(a.n_m, UG_BM / UG_ROWS_PER_CTA);
-  ug_bits_kernel<<<pgrid, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 4, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  if (own_bits) {
+    ug_bits_kernel<<<pgrid, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 4, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  }
   ug_scan_kernel<<<a.n_m, UG_PREP_THREADS, static_cast<size_t>(L.nw) * 8, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
   if (!Wd_f16) {
@@ -1052,4 +1085,24 @@ extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
   }
   if ((st = ug_launch<UG_UP>(map_x, map_as, a, a.n_m * a.nj, dev, s)) != TWELL_OK) return st;
   return ug_launch<UG_DOWN>(map_a, map_y, a, a.n_m * a.nN, dev, s);
+}
+
+}  // namespace
+}  // namespace twell
+
+extern "C" twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h,
+                                         const uint16_t* Wu_t, const uint16_t* Wd,
+                                         const uint16_t* Wd_f16, int32_t D, float* y, void* ws,
+                                         size_t ws_bytes, int32_t* status_dev, void* stream) {
+  return twell::ffn_tc_run(x, h, Wu_t, Wd, Wd_f16, D, y, ws, ws_bytes, status_dev, stream,
+                           false);
+}
+
+extern "C" twell_status twell_ffn_fwd_tc_sorted(const uint16_t* x, const twell_t* h,
+                                                const uint16_t* Wu_t, const uint16_t* Wd,
+                                                const uint16_t* Wd_f16, int32_t D, float* y,
+                                                void* ws, size_t ws_bytes, int32_t* status_dev,
+                                                void* stream) {
+  return twell::ffn_tc_run(x, h, Wu_t, Wd, Wd_f16, D, y, ws, ws_bytes, status_dev, stream,
+                           true);
 }

@@ -41,7 +41,8 @@ struct Entry {
 // of a hybrid (ell = true; n_rows / ell_rows / u_save set, W = C, no spill).
 twell_status launch_fused(const FfnParams& p, const DeviceInfo& dev, cudaStream_t s, bool ell);
 
-// Workspace bytes of twell_ffn_fwd_tc for T rows, width D and F gate columns.
-size_t ffn_tc_workspace_bytes(int64_t T, int64_t D, int64_t F);
+// Workspace bytes of twell_ffn_fwd_tc (sorted: twell_ffn_fwd_tc_sorted) for T
+// rows, width D and F gate columns.
+size_t ffn_tc_workspace_bytes(int64_t T, int64_t D, int64_t F, bool sorted);
 
 }  // namespace twell

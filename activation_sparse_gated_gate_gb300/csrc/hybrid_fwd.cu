@@ -16,8 +16,10 @@
 
 extern "C" size_t twell_workspace_size(int32_t op, int32_t T, int32_t D, int32_t F,
                                        int32_t cap, int32_t max_dense) {
-  if (op == TWELL_WS_FFN_FWD_TC)
-    return T < 0 || D <= 0 || F <= 0 ? 0 : twell::ffn_tc_workspace_bytes(T, D, F);
+  if (op == TWELL_WS_FFN_FWD_TC || op == TWELL_WS_FFN_FWD_TC_SORTED)
+    return T < 0 || D <= 0 || F <= 0
+               ? 0
+               : twell::ffn_tc_workspace_bytes(T, D, F, op == TWELL_WS_FFN_FWD_TC_SORTED);
   if (op < 1 || op > 4 || T < 0 || D <= 0 || F <= 0 || cap < 1 || max_dense < 0) return 0;
   return twell::ws_layout(op, T, D, F, cap, max_dense).bytes;
 }

@@ -595,6 +595,10 @@ class InferCase:
         self.y_cc = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
         self.ws_tc = torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC, w.T, w.D, w.F, 0,
                                                           0),), dtype=torch.uint8, device=dev)
+        self.y_tcs = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+        self.ws_tcs = torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC_SORTED, w.T, w.D,
+                                                           w.F, 0, 0),),
+                                  dtype=torch.uint8, device=dev)
         # the tensor-core forward's down GEMM takes W_d in fp16: converted once
         # per model, like any weight preparation, outside the timed steps
         self.Wd16 = tw.twell_to_f16(self.Wd)
@@ -608,9 +612,17 @@ class InferCase:
         tw.twell_ffn_fwd_tc(self.x, self.h, self.Wu, self.Wd, y=self.y, ws=self.ws_tc,
                             Wd_f16=self.Wd16, stream=self.stream)
 
+    def fwd_tcs(self):
+        import activation_sparse_gated_gate_gb300 as tw
+        tw.twell_ffn_fwd_tc_sorted(self.x, self.h, self.Wu, self.Wd, y=self.y_tcs,
+                                   ws=self.ws_tcs, Wd_f16=self.Wd16, stream=self.stream)
+
     def fwd_cc(self):
         import activation_sparse_gated_gate_gb300 as tw
         tw.twell_ffn_fwd(self.x, self.h, self.Wu, self.Wd, y=self.y_cc, stream=self.stream)
+
+    def fwd(self, kind):
+        {"tc": self.fwd_tc, "tcs": self.fwd_tcs, "cc": self.fwd_cc}[kind]()
 
     def active_union(self):
         """Neurons active in some row (one untimed pack with z exported)."""
@@ -623,79 +635,82 @@ class InferCase:
         return n
 
 
+FWD_NAMES = {"tc": "twell_ffn_fwd_tc", "tcs": "twell_ffn_fwd_tc_sorted", "cc": "twell_ffn_fwd"}
+# kernels of the library launched by one step (gate + forward), for
+# gpu_launches: the gate kernel, then union scan + up + down GEMMs; the
+# sorted variant adds three sort kernels, the x copy and the union bitmaps;
+# the CUDA-core forward is one kernel
+STEP_LAUNCHES = {"tc": 4, "tcs": 9, "cc": 2}
+
+
 def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", clk=None):
-    """Time one inference workload: K iterations, each running the step with
-    the tensor-core forward and the step with the CUDA-core fused kernel,
-    each after its own L2 flush, with events around every call.  Returns the
-    entry dict (times, tokens/s, rooflines) and the raw per-step times."""
+    """Time one inference workload: K iterations, each running the step
+    with each forward (tensor-core, tensor-core on activity-sorted blocks,
+    CUDA-core fused), each after its own L2 flush, with events around every
+    call.  Returns the entry dict (times, tokens/s, rooflines) and the raw
+    per-step times."""
     import torch
     w = case.w
     stream = case.stream
     hbm, bf16, _, src = peaks
+    kinds = ("tc", "tcs", "cc")
     n_active = case.active_union()
     for _ in range(warmup):
-        flush.zero_()
-        case.gate()
-        case.fwd_tc()
-        flush.zero_()
-        case.gate()
-        case.fwd_cc()
+        for kd in kinds:
+            flush.zero_()
+            case.gate()
+            case.fwd(kd)
     torch.cuda.synchronize()
     if int(case.h.status.item()) != 0:
         raise RuntimeError(f"device status flags {int(case.h.status.item())} ({w.name})")
     K = steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    ev = {kd: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+          for kd in kinds}
     torch.cuda.synchronize()
     for i in range(K):
-        flush.zero_()
-        ev[i][0].record(stream)
-        case.gate()
-        ev[i][1].record(stream)
-        case.fwd_tc()
-        ev[i][2].record(stream)
-        flush.zero_()
-        ev[i][3].record(stream)
-        case.gate()
-        ev[i][4].record(stream)
-        case.fwd_cc()
-        ev[i][5].record(stream)
+        for kd in kinds:
+            e = ev[kd][i]
+            flush.zero_()
+            e[0].record(stream)
+            case.gate()
+            e[1].record(stream)
+            case.fwd(kd)
+            e[2].record(stream)
     torch.cuda.synchronize()
     if int(case.h.status.item()) != 0:
         raise RuntimeError(f"device status flags {int(case.h.status.item())} ({w.name})")
-    t_g = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    t_tc = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    t_gc = [ev[i][3].elapsed_time(ev[i][4]) for i in range(K)]
-    t_cc = [ev[i][4].elapsed_time(ev[i][5]) for i in range(K)]
-    tc_step = max_over_ranks(sum(a + b for a, b in zip(t_g, t_tc)) / K, case.dev)
-    cc_step = max_over_ranks(sum(a + b for a, b in zip(t_gc, t_cc)) / K, case.dev)
-    use_tc = tc_step <= cc_step if forward == "auto" else forward == "tc"
-    rel = float((case.y - case.y_cc).norm() / max(float(case.y_cc.norm()), 1e-30))
-    if not rel < 5e-3:
-        raise RuntimeError(f"tensor-core and CUDA-core forwards differ (relative {rel:.2e}, "
-                           f"{w.name})")
+    t_gate = [ev[kd][i][0].elapsed_time(ev[kd][i][1]) for kd in kinds for i in range(K)]
+    t_fwd = {kd: [ev[kd][i][1].elapsed_time(ev[kd][i][2]) for i in range(K)] for kd in kinds}
+    step = {kd: max_over_ranks(sum(ev[kd][i][0].elapsed_time(ev[kd][i][2]) for i in range(K)) / K,
+                               case.dev) for kd in kinds}
+    best = min(step, key=step.get) if forward == "auto" else forward
+    for kd, yk in (("tc", case.y), ("tcs", case.y_tcs)):
+        rel = float((yk - case.y_cc).norm() / max(float(case.y_cc.norm()), 1e-30))
+        if not rel < 5e-3:
+            raise RuntimeError(f"{FWD_NAMES[kd]} and the CUDA-core forward differ (relative "
+                               f"{rel:.2e}, {w.name})")
     nnz = int(case.h.cnt.to(torch.int64).sum().item())
     union_sum = _block_unions(case.h, w.T, w.F)
-    g_ms = statistics.mean(t_g + t_gc)
-    tc_ms = statistics.mean(t_tc)
-    cc_ms = statistics.mean(t_cc)
-    ms_step = tc_step if use_tc else cc_step
+    g_ms = statistics.mean(t_gate)
+    fwd_ms = {kd: statistics.mean(t_fwd[kd]) for kd in kinds}
+    ms_step = step[best]
     ws_n = int(os.environ.get("WORLD_SIZE", "1"))
-    gate = gate_roofline(w.T, w.D, w.F, nnz, g_ms, hbm, bf16)
-    r_tc = updown_roofline(w.T, w.D, w.F, nnz, n_active, tc_ms, hbm, fma, bf16, union_sum)
-    r_cc = updown_roofline(w.T, w.D, w.F, nnz, n_active, cc_ms, hbm, fma)
-    fwd_name = "twell_ffn_fwd_tc" if use_tc else "twell_ffn_fwd"
+    kernels = {"twell_gate_pack": gate_roofline(w.T, w.D, w.F, nnz, g_ms, hbm, bf16)}
+    for kd in kinds:
+        kernels[FWD_NAMES[kd]] = updown_roofline(
+            w.T, w.D, w.F, nnz, n_active, fwd_ms[kd], hbm, fma, bf16,
+            union_sum if kd == "tc" else None)
     entry = {
         "workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F, "twell_width": w.width,
         "nnz": nnz, "density": nnz / (w.T * w.F), "active_neurons": n_active,
         "block_union_mean": union_sum / ((w.T + 127) // 128),
         "tokens_per_s": job_tokens_per_s(w.T, ws_n, ms_step), "ms_per_step": ms_step,
-        "forward": fwd_name,
-        "steps": {"tensor_core_ms": tc_step, "cuda_core_ms": cc_step},
-        "kernels": {"twell_gate_pack": gate, "twell_ffn_fwd_tc": r_tc, "twell_ffn_fwd": r_cc},
-        "relative_difference_tc_cc": rel,
+        "forward": FWD_NAMES[best],
+        "steps_ms": {FWD_NAMES[kd]: step[kd] for kd in kinds},
+        "kernels": kernels,
     }
-    return entry, {"use_tc": use_tc, "fwd_ms": tc_ms if use_tc else cc_ms, "gate_ms": g_ms,
-                   "fwd_name": fwd_name, "nnz": nnz, "n_active": n_active,
+    return entry, {"use": best, "fwd_ms": fwd_ms[best], "gate_ms": g_ms,
+                   "fwd_name": FWD_NAMES[best], "nnz": nnz, "n_active": n_active,
                    "union_sum": union_sum}
 
 
@@ -1014,45 +1029,46 @@ def e2e_pipeline(args, case, flush, K):
     chunk_state = {}
 
     def chunk_bufs(n):
-        # a TwELL and a tensor-core workspace per chunk (sized for n tokens)
+        # a TwELL and a tensor-core workspace per chunk (sized for n tokens
+        # and either tensor-core forward)
         h_c = tw.TwELL(n, w.F, w.width, device=dev)
-        ws_c = torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC, n, w.D, w.F, 0, 0),),
-                           dtype=torch.uint8, device=dev)
+        ws_c = torch.empty((tw.twell_workspace_size(tw.WS_FFN_FWD_TC_SORTED, n, w.D, w.F, 0,
+                                                    0),), dtype=torch.uint8, device=dev)
         return h_c, ws_c
 
-    def chunk_fwd(a, b, hc, fwd_tc, st):
+    def chunk_fwd(a, b, hc, kind, st):
         tw.twell_gate_pack(x[a:b], Wg, hc[0], stream=st)
-        if fwd_tc:
-            tw.twell_ffn_fwd_tc(x[a:b], hc[0], Wu, Wd, y=y[a:b], ws=hc[1], Wd_f16=Wd16,
-                                stream=st)
-        else:
+        if kind == "cc":
             tw.twell_ffn_fwd(x[a:b], hc[0], Wu, Wd, y=y[a:b], stream=st)
+        else:
+            tw.twell_ffn_fwd_tc(x[a:b], hc[0], Wu, Wd, y=y[a:b], ws=hc[1], Wd_f16=Wd16,
+                                stream=st, sorted_rows=kind == "tcs")
 
-    def chunk_ms(n, fwd_tc):
+    def chunk_ms(n, kind):
         # one chunk of n tokens, device-resident, mean of 3 after a warm-up
-        key = (n, fwd_tc)
+        key = (n, kind)
         if key not in chunk_state:
             hc = chunk_bufs(n)
             c_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
             for it in range(4):
                 if it == 1:
                     c_ev[0].record(stream)
-                chunk_fwd(0, n, hc, fwd_tc, stream)
+                chunk_fwd(0, n, hc, kind, stream)
             c_ev[1].record(stream)
             torch.cuda.synchronize()
             chunk_state[key] = c_ev[0].elapsed_time(c_ev[1]) / 3
         return chunk_state[key]
 
-    def use_tc_for(n):
+    def kind_for(n):
         if args.forward != "auto":
-            return args.forward == "tc"
-        return chunk_ms(n, True) <= chunk_ms(n, False)
+            return args.forward
+        return min(("tc", "tcs", "cc"), key=lambda kd: chunk_ms(n, kd))
 
     def build_plan(parts):
         sizes = plan_sizes(w.T, parts)
         bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
         bufs = [chunk_bufs(n) for n in sizes]
-        fwds = [use_tc_for(n) for n in sizes]
+        fwds = [kind_for(n) for n in sizes]
 
         def pipelined_step(origin):
             # fork from `origin`, one chunk per stage on each stream, join back
@@ -1109,7 +1125,7 @@ def e2e_pipeline(args, case, flush, K):
             "pipeline": (f"token chunks {plan['sizes']} (plan {plan_name}, the fastest of "
                          f"{len(plans)} tried untimed), copy-in / compute / copy-out streams, "
                          "replayed as one CUDA graph"),
-            "forward": [("tensor-core" if f else "CUDA-core") for f in plan["fwds"]],
+            "forward": [FWD_NAMES[f] for f in plan["fwds"]],
             "forward_choice": ("per chunk, the faster measured at its size"
                                if args.forward == "auto"
                                else f"fixed by --forward {args.forward}"),
@@ -1155,8 +1171,7 @@ def run_ours(args, head_cfg):
     e2e = None if args.no_e2e else e2e_pipeline(args, case, flush, K)
     energy = None
     if not args.no_energy:
-        step = (lambda: (case.gate(), case.fwd_tc())) if raw["use_tc"] else \
-            (lambda: (case.gate(), case.fwd_cc()))
+        step = lambda: (case.gate(), case.fwd(raw["use"]))
         e_ours = energy_per_token(step, w.T, stream, local)
         e_dense = energy_per_token(
             lambda: (torch.relu(case.x @ case.Wg.t()) * (case.x @ case.Wu.t())) @ case.Wd,
@@ -1188,7 +1203,7 @@ def run_ours(args, head_cfg):
 
     value = entry["tokens_per_s"]
     ms_step = entry["ms_per_step"]
-    use_tc = raw["use_tc"]
+    use_tc = raw["use"] != "cc"
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -1206,17 +1221,15 @@ def run_ours(args, head_cfg):
                                "copy of W_d is made once per model (twell_to_f16) outside the "
                                "timed region")},
         "e2e": e2e,
-        # our kernels in the headline's timed region per iteration: gate, union
-        # scan, up and down GEMMs (tensor-core step) + gate and fused kernel
-        # (CUDA-core step)
-        "gpu_launches": 6 * K,
+        # our kernels in the headline's timed region: every iteration runs the
+        # step with each of the three forwards
+        "gpu_launches": K * sum(STEP_LAUNCHES.values()),
         "roofline": roof,
         "headline": entry,
         "configs": configs,
         "fma_peak": fma_meta,
-        "forward": ("tensor-core union gather (twell_ffn_fwd_tc)" if use_tc
-                    else "CUDA-core fused kernel (twell_ffn_fwd)"),
-        "forward_choice": ("the faster of the two measured steps" if args.forward == "auto"
+        "forward": raw["fwd_name"],
+        "forward_choice": ("the fastest of the three measured steps" if args.forward == "auto"
                            else f"fixed by --forward {args.forward}"),
         "energy": energy,
         "clocks": clk_sum,
@@ -1255,7 +1268,7 @@ def main():
     ap.add_argument("--train-steps", type=int, default=5)
     ap.add_argument("--no-energy", action="store_true", help="skip the energy-per-token section")
     ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack section")
-    ap.add_argument("--forward", default="auto", choices=["auto", "tc", "cc"],
+    ap.add_argument("--forward", default="auto", choices=["auto", "tc", "tcs", "cc"],
                     help="inference forward of the steps and the end-to-end pipeline: the "
                          "faster measured one (auto) or a fixed one (profiling runs, where a "
                          "profiler's per-launch overhead distorts the comparison)")

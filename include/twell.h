@@ -164,12 +164,9 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
 /*
  * Tensor-core variant of twell_ffn_fwd (paper section 2.B.2: up and down
  * projections of the active neurons only, built to keep the tensor cores
- * busy).  Same function, different arithmetic: the rows are first ordered by
- * their count of active neurons (a stable sort into eight buckets per octave;
- * blocks of rows with similar activity have smaller unions), then for each
- * block of 128 rows in that order the union U of the rows' active neurons
- * (built from the slots and spill slices; h->block_bits is not read) is
- * gathered, u = x W_u[:, U] is
+ * busy).  Same function, different arithmetic: for each block of 128 rows
+ * the union U of the rows' active neurons (h->block_bits when it is not
+ * NULL, else built from the slots and spill slices) is gathered, u = x W_u[:, U] is
  * one tcgen05 GEMM (bf16 in, fp32 out), a = h u is rounded to fp16 at each
  * row's own active neurons (0 at the union's other positions), and
  * y = a W_d[U, :] is a second tcgen05 GEMM on fp16 operands (W_d converted
@@ -183,9 +180,9 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
  *   Wd_f16  optional [F][D] fp16 copy of Wd (twell_to_f16); NULL: the call
  *           makes one in the workspace (one extra pass over W_d)
  *   ws: twell_workspace_size(TWELL_WS_FFN_FWD_TC, T, D, F, 0, 0) bytes,
- *       256-byte aligned (the row order, x in that order, per-block unions
- *       and position prefixes, the [T][F] fp16 matrix of a in union order
- *       and the fp16 copy of W_d: about 2 (T + D) F + 2 T D bytes)
+ *       256-byte aligned (per-block unions and position prefixes, the
+ *       [T][F] fp16 matrix of a in union order and the fp16 copy of W_d:
+ *       about 2 (T + D) F bytes)
  * A (row, tile) whose spill slice is missing is skipped and
  * TWELL_FLAG_SPILL_FULL is set.  Results do not depend on how the work is
  * scheduled: repeated calls agree bit for bit.  T may be 0.
@@ -195,6 +192,28 @@ twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* 
 twell_status twell_ffn_fwd_tc(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
                               const uint16_t* Wd, const uint16_t* Wd_f16, int32_t D, float* y,
                               void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * twell_ffn_fwd_tc over blocks of rows grouped by activity: the rows are
+ * first ordered by their count of active neurons (a stable sort into eight
+ * buckets per octave of the count), then every block of 128 rows in that
+ * order is processed as in twell_ffn_fwd_tc (h->block_bits is not read; the
+ * blocks' unions are built from the slots and spill slices) and each y row
+ * is written to its own token.  A block's union grows with its rows'
+ * summed activity in a concave way, so when the per-row activity varies
+ * widely (a heavy-tailed batch) the sorted blocks have a much smaller total
+ * union and the GEMMs less work; when every row is about equally active
+ * the sort and the copy of x in sorted order only add time.  Same
+ * arguments, results and errors as twell_ffn_fwd_tc; the workspace is
+ * twell_workspace_size(TWELL_WS_FFN_FWD_TC_SORTED, T, D, F, 0, 0) bytes (that
+ * of twell_ffn_fwd_tc plus the row order and a copy of x: + 2 T D + 5 T
+ * bytes and a little more).  Rows are summed in an order fixed by the data,
+ * so repeated calls agree bit for bit.
+ */
+twell_status twell_ffn_fwd_tc_sorted(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
+                                     const uint16_t* Wd, const uint16_t* Wd_f16, int32_t D,
+                                     float* y, void* ws, size_t ws_bytes, int32_t* status_dev,
+                                     void* stream);
 
 /*
  * fp16 copy of bf16 values (for the W_d operand of twell_ffn_fwd_tc, made
@@ -263,7 +282,8 @@ enum {
   TWELL_WS_HYBRID_BWD = 2,
   TWELL_WS_HYBRID_FWD_TC = 3,
   TWELL_WS_HYBRID_BWD_TC = 4,
-  TWELL_WS_FFN_FWD_TC = 5  /* twell_ffn_fwd_tc; cap and max_dense are ignored */
+  TWELL_WS_FFN_FWD_TC = 5,        /* twell_ffn_fwd_tc; cap and max_dense are ignored */
+  TWELL_WS_FFN_FWD_TC_SORTED = 6  /* twell_ffn_fwd_tc_sorted; cap and max_dense ignored */
 };
 
 /*

@@ -140,6 +140,9 @@ def test_workspace_sizes(lib):
         assert tw.twell_workspace_size(op, T, D, F, 0, MD) == 0
         assert tw.twell_workspace_size(op, T, D, F, C, -1) == 0
     assert tw.twell_workspace_size(0, T, D, F, C, MD) == 0
-    assert tw.twell_workspace_size(6, T, D, F, C, MD) == 0
+    # the sorted tensor-core forward adds the row order and x in that order
+    assert tw.twell_workspace_size(tw.WS_FFN_FWD_TC_SORTED, 8192, 1536, 6144, 0, 0) >= \
+        tw.twell_workspace_size(tw.WS_FFN_FWD_TC, 8192, 1536, 6144, 0, 0) + 8192 * (2 * 1536 + 5)
+    assert tw.twell_workspace_size(7, T, D, F, C, MD) == 0
     # T = 0 needs no per-row buffers but stays a valid request
     assert tw.twell_workspace_size(tw.WS_HYBRID_BWD_TC, 0, D, F, C, MD) >= 3 * fd

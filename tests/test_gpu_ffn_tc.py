@@ -236,3 +236,57 @@ def test_config_full_size(idx):
     ri = torch.as_tensor(rows, device="cuda")
     zg = z[ri].cpu().numpy()
     check_y_tc(y[ri].cpu().numpy().astype(np.float64), w, zg, rows)
+
+
+# ------------------------------------------- blocks grouped by activity (sorted)
+
+def _tc_sorted(d, h, w):
+    return tw.twell_ffn_fwd_tc_sorted(d["x"], h, d["Wu_t"], d["Wd"])
+
+
+@pytest.mark.parametrize("T,D,F,p,W", CASES)
+def test_ffn_fwd_tc_sorted_parity(T, D, F, p, W):
+    w = workloads.random_small(T, D, F, p, W, seed=T + D + 1)
+    d, h, z = run_pack(w)
+    y = _tc_sorted(d, h, w)
+    torch.cuda.synchronize()
+    assert int(h.status.item()) == 0
+    check_y_tc(y.cpu().numpy().astype(np.float64), w, z.cpu().numpy())
+
+
+def test_sorted_heavy_tail_repeats_and_agrees_with_token_order():
+    # per-token activity spread like the 1.5B-class workload (lognormal
+    # threshold offsets): the sorted blocks give the same y as blocks of
+    # consecutive tokens up to fp16 rounding of h u, and repeats are equal
+    w = workloads.make_heavy_tail("heavy-tail small", 3000, 256, 2048, 0.01, 16, seed=4)
+    d, h, z = run_pack(w)
+    y1 = _tc_sorted(d, h, w)
+    y2 = _tc_sorted(d, h, w)
+    y0 = tw.twell_ffn_fwd_tc(d["x"], h, d["Wu_t"], d["Wd"])
+    torch.cuda.synchronize()
+    assert int(h.status.item()) == 0
+    assert torch.equal(y1, y2)
+    assert float((y1 - y0).norm() / y0.norm()) <= 2e-3
+    check_y_tc(y1.cpu().numpy().astype(np.float64), w, z.cpu().numpy())
+
+
+def test_sorted_spill_capacity_exhausted_sets_flag():
+    w = workloads.random_small(256, 128, 1024, 0.5, 8, seed=5)
+    d, h, z = run_pack(w, spill_cap=4)
+    _tc_sorted(d, h, w)
+    torch.cuda.synchronize()
+    assert int(h.status.item()) & tw.FLAG_SPILL_FULL
+
+
+def test_sorted_full_size_heavy_tail_layer():
+    # the 1.5B-class layer at full size in the bench's launch configuration,
+    # checked on sampled rows
+    w = workloads.config(2)
+    d, h, z = run_pack(w)
+    y = _tc_sorted(d, h, w)
+    torch.cuda.synchronize()
+    assert int(h.status.item()) == 0
+    rng = np.random.default_rng(2)
+    rows = np.sort(np.concatenate([rng.choice(w.T, 96, replace=False), [0, w.T - 1]]))
+    idx = torch.as_tensor(rows, device="cuda")
+    check_y_tc(y[idx].cpu().numpy().astype(np.float64), w, z[idx].cpu().numpy(), rows)
