@@ -59,13 +59,24 @@ METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of ro
 # the committed ncu captures in profiles/, valid only while the kernel's source
 # is the one captured (sha256 of the .cu file); otherwise reported as null.
 TRAFFIC = {
-    ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        108.88e6, "csrc/ffn_fwd.cu", "fdba64ead7a8eeb0", "profiles/ffn_fwd_0.5B_T8192.md"),
-    ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        44.64e6, "csrc/gate_pack.cu", "7161047be7ce0d3d", "profiles/gate_pack_0.5B_T8192.md"),
-    # the call's three kernels (union scan, up and down GEMMs)
+    # 1.5B-class layer (profiles/ffn_fwd_tc_1.5B_T16384.md)
+    ("twell_ffn_fwd_tc_sorted", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
+        730.17e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    ("twell_ffn_fwd_tc", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
+        789.17e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
+        776.32e6, "csrc/ffn_fwd.cu", "413694b7d064fc5c", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
+        149.88e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        216.6e6, "csrc/ffn_tc.cu", "484e1de77c067100", "profiles/ffn_fwd_tc_0.5B_T8192.md"),
+        211.39e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    ("twell_ffn_fwd_tc_sorted", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
+        237.81e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
+        106.01e6, "csrc/ffn_fwd.cu", "413694b7d064fc5c", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+    ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
+        45.03e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
 
 
