@@ -614,26 +614,28 @@ class InferCase:
         # per model, like any weight preparation, outside the timed steps
         self.Wd16 = tw.twell_to_f16(self.Wd)
 
-    def gate(self):
+    def gate(self, stream=None):
         import activation_sparse_gated_gate_gb300 as tw
-        tw.twell_gate_pack(self.x, self.Wg, self.h, stream=self.stream)
+        tw.twell_gate_pack(self.x, self.Wg, self.h, stream=stream or self.stream)
 
-    def fwd_tc(self):
+    def fwd_tc(self, stream=None):
         import activation_sparse_gated_gate_gb300 as tw
         tw.twell_ffn_fwd_tc(self.x, self.h, self.Wu, self.Wd, y=self.y, ws=self.ws_tc,
-                            Wd_f16=self.Wd16, stream=self.stream)
+                            Wd_f16=self.Wd16, stream=stream or self.stream)
 
-    def fwd_tcs(self):
+    def fwd_tcs(self, stream=None):
         import activation_sparse_gated_gate_gb300 as tw
         tw.twell_ffn_fwd_tc_sorted(self.x, self.h, self.Wu, self.Wd, y=self.y_tcs,
-                                   ws=self.ws_tcs, Wd_f16=self.Wd16, stream=self.stream)
+                                   ws=self.ws_tcs, Wd_f16=self.Wd16,
+                                   stream=stream or self.stream)
 
-    def fwd_cc(self):
+    def fwd_cc(self, stream=None):
         import activation_sparse_gated_gate_gb300 as tw
-        tw.twell_ffn_fwd(self.x, self.h, self.Wu, self.Wd, y=self.y_cc, stream=self.stream)
+        tw.twell_ffn_fwd(self.x, self.h, self.Wu, self.Wd, y=self.y_cc,
+                         stream=stream or self.stream)
 
-    def fwd(self, kind):
-        {"tc": self.fwd_tc, "tcs": self.fwd_tcs, "cc": self.fwd_cc}[kind]()
+    def fwd(self, kind, stream=None):
+        {"tc": self.fwd_tc, "tcs": self.fwd_tcs, "cc": self.fwd_cc}[kind](stream)
 
     def active_union(self):
         """Neurons active in some row (one untimed pack with z exported)."""
@@ -647,53 +649,76 @@ class InferCase:
 
 
 FWD_NAMES = {"tc": "twell_ffn_fwd_tc", "tcs": "twell_ffn_fwd_tc_sorted", "cc": "twell_ffn_fwd"}
-# kernels of the library launched by one step (gate + forward), for
-# gpu_launches: the gate kernel, then union scan + up + down GEMMs; the
-# sorted variant adds three sort kernels, the x copy and the union bitmaps;
-# the CUDA-core forward is one kernel
-STEP_LAUNCHES = {"tc": 4, "tcs": 9, "cc": 2}
+# kernels of the library launched by one forward call: union scan + up +
+# down GEMMs; the sorted variant adds three sort kernels, the x copy and the
+# union bitmaps; the CUDA-core forward is one kernel (the gate is one more)
+FWD_LAUNCHES = {"tc": 3, "tcs": 8, "cc": 1}
+# per timed iteration of infer_entry: the gate graph, each forward's graph
+# and each step's graph (gate + forward)
+ITER_LAUNCHES = 1 + sum(FWD_LAUNCHES.values()) + sum(1 + n for n in FWD_LAUNCHES.values())
+
+
+def _capture(dev, fn):
+    """A CUDA graph of fn() captured on a side stream (one warm-up call
+    first, so per-call setup such as kernel attributes happens outside)."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fn(side)
+    torch.cuda.synchronize()
+    return g
 
 
 def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", clk=None):
-    """Time one inference workload: K iterations, each running the step
-    with each forward (tensor-core, tensor-core on activity-sorted blocks,
-    CUDA-core fused), each after its own L2 flush, with events around every
-    call.  Returns the entry dict (times, tokens/s, rooflines) and the raw
-    per-step times."""
+    """Time one inference workload.  Each call (the gate; each forward:
+    tensor-core, tensor-core on activity-sorted blocks, CUDA-core fused) and
+    each step (the gate followed by one forward) is captured once as a CUDA
+    graph and replayed, after an L2 flush, between CUDA events on the
+    launching stream: graph replay keeps the GPU's per-launch processing
+    (several microseconds per kernel or memset issued one by one) out of the
+    decode-sized calls, as a decode loop would.  K iterations run every graph
+    once.  Returns the entry dict (times, tokens/s, rooflines) and the raw
+    times."""
     import torch
     w = case.w
     stream = case.stream
     hbm, bf16, _, src = peaks
     kinds = ("tc", "tcs", "cc")
     n_active = case.active_union()
+    graphs = {"gate": _capture(case.dev, lambda st: case.gate(st))}
+    for kd in kinds:
+        graphs[kd] = _capture(case.dev, lambda st, kd=kd: case.fwd(kd, st))
+        graphs["step_" + kd] = _capture(case.dev,
+                                        lambda st, kd=kd: (case.gate(st), case.fwd(kd, st)))
+    order = ["gate"] + [k for kd in kinds for k in (kd, "step_" + kd)]
     for _ in range(warmup):
-        for kd in kinds:
+        for name in order:
             flush.zero_()
-            case.gate()
-            case.fwd(kd)
+            graphs[name].replay()
     torch.cuda.synchronize()
     if int(case.h.status.item()) != 0:
         raise RuntimeError(f"device status flags {int(case.h.status.item())} ({w.name})")
     K = steps
-    ev = {kd: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-          for kd in kinds}
-    torch.cuda.synchronize()
+    ev = {name: [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+          for name in order}
     for i in range(K):
-        for kd in kinds:
-            e = ev[kd][i]
+        for name in order:
+            e = ev[name][i]
             flush.zero_()
             e[0].record(stream)
-            case.gate()
+            graphs[name].replay()
             e[1].record(stream)
-            case.fwd(kd)
-            e[2].record(stream)
     torch.cuda.synchronize()
     if int(case.h.status.item()) != 0:
         raise RuntimeError(f"device status flags {int(case.h.status.item())} ({w.name})")
-    t_gate = [ev[kd][i][0].elapsed_time(ev[kd][i][1]) for kd in kinds for i in range(K)]
-    t_fwd = {kd: [ev[kd][i][1].elapsed_time(ev[kd][i][2]) for i in range(K)] for kd in kinds}
-    step = {kd: max_over_ranks(sum(ev[kd][i][0].elapsed_time(ev[kd][i][2]) for i in range(K)) / K,
-                               case.dev) for kd in kinds}
+    t = {name: statistics.mean(ev[name][i][0].elapsed_time(ev[name][i][1]) for i in range(K))
+         for name in order}
+    step = {kd: max_over_ranks(t["step_" + kd], case.dev) for kd in kinds}
     best = min(step, key=step.get) if forward == "auto" else forward
     for kd, yk in (("tc", case.y), ("tcs", case.y_tcs)):
         rel = float((yk - case.y_cc).norm() / max(float(case.y_cc.norm()), 1e-30))
@@ -702,14 +727,13 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
                                f"{rel:.2e}, {w.name})")
     nnz = int(case.h.cnt.to(torch.int64).sum().item())
     union_sum = _block_unions(case.h, w.T, w.F)
-    g_ms = statistics.mean(t_gate)
-    fwd_ms = {kd: statistics.mean(t_fwd[kd]) for kd in kinds}
+    g_ms = t["gate"]
     ms_step = step[best]
     ws_n = int(os.environ.get("WORLD_SIZE", "1"))
     kernels = {"twell_gate_pack": gate_roofline(w.T, w.D, w.F, nnz, g_ms, hbm, bf16)}
     for kd in kinds:
         kernels[FWD_NAMES[kd]] = updown_roofline(
-            w.T, w.D, w.F, nnz, n_active, fwd_ms[kd], hbm, fma, bf16,
+            w.T, w.D, w.F, nnz, n_active, t[kd], hbm, fma, bf16,
             union_sum if kd == "tc" else None)
     entry = {
         "workload": w.name, "T": w.T, "d_model": w.D, "d_ff": w.F, "twell_width": w.width,
@@ -719,8 +743,10 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
         "forward": FWD_NAMES[best],
         "steps_ms": {FWD_NAMES[kd]: step[kd] for kd in kinds},
         "kernels": kernels,
+        "timing": ("each call and each step captured as a CUDA graph, replayed after an L2 "
+                   "flush between CUDA events; mean of K"),
     }
-    return entry, {"use": best, "fwd_ms": fwd_ms[best], "gate_ms": g_ms,
+    return entry, {"use": best, "fwd_ms": t[best], "gate_ms": g_ms,
                    "fwd_name": FWD_NAMES[best], "nnz": nnz, "n_active": n_active,
                    "union_sum": union_sum}
 
@@ -1232,9 +1258,9 @@ def run_ours(args, head_cfg):
                                "copy of W_d is made once per model (twell_to_f16) outside the "
                                "timed region")},
         "e2e": e2e,
-        # our kernels in the headline's timed region: every iteration runs the
-        # step with each of the three forwards
-        "gpu_launches": K * sum(STEP_LAUNCHES.values()),
+        # our kernels in the headline's timed region: every iteration replays
+        # the gate, each forward and each step once
+        "gpu_launches": K * ITER_LAUNCHES,
         "roofline": roof,
         "headline": entry,
         "configs": configs,
