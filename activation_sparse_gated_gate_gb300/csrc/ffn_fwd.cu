@@ -238,7 +238,16 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
           const int s = static_cast<int>(n_i % static_cast<uint32_t>(P));
           // warp-uniform decision: the lanes shuffle together below
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars[s], (n_i / P) & 1u))) {
-            if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            // before leaving, wait (bounded) for the row copies this warp
+            // still has in flight into its stages: entries i .. i + P - 1
+            if (lane == 0) {
+              atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+              for (int r = i; r < min(m, i + P); ++r) {
+                const uint32_t n_r = seq + r;
+                if (!ptx::mbar_wait(&bars[n_r % static_cast<uint32_t>(P)], (n_r / P) & 1u)) break;
+              }
+            }
+            __syncwarp();
             return;
           }
           const Entry e = list[i];

@@ -53,7 +53,10 @@
 //               (32 copies per thread), marking it full once its copies
 //               have landed and it has fenced them to the async proxy
 // Every wait is bounded (about a second); a wait that runs out sets
-// TWELL_FLAG_TIMEOUT and the CTA leaves its loops, frees its TMEM and exits.
+// TWELL_FLAG_TIMEOUT and the CTA leaves its loops; before it frees its TMEM
+// and exits, every MMA it issued completes (a commit to a barrier of its
+// own, waited for) and the TMA loads it issued land (a bounded 100 us wait:
+// their completion barrier may no longer complete once another role left).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -566,6 +569,8 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
   uint64_t* tfull = empty + UG_ST;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // abort path: MMA drain
+  volatile uint32_t* aborted = tmem_slot + 1;
   float* hslots = reinterpret_cast<float*>(smem + SM::SLOTS);  // up: [2][128][UG_HSLOTS]
 
   const int warp = threadIdx.x >> 5;
@@ -584,6 +589,8 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], UG_EPI);
     }
+    ptx::mbar_init(drain, 1);
+    *aborted = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -606,7 +613,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
         for (int kb = 0; kb < U.kb; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
-            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
             goto done;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], UG_A);
@@ -637,14 +644,14 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
         const uint32_t acc_phase = (local >> 1) & 1;
         ++local;
         if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
-          atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
           goto done;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * UG_BN);
         for (int kb = 0; kb < U.kb; ++kb) {
           if (!ptx::mbar_wait(&full[stage], phase)) {
-            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
             goto done;
           }
           ptx::tc_fence_after();
@@ -720,7 +727,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       for (; kb < U.kb; kb += UG_ST) {
         const uint32_t phase = static_cast<uint32_t>((seq0 + kb) / UG_ST) & 1u;
         if (!ptx::mbar_wait(eb, phase ^ 1u)) {
-          atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
           goto done;
         }
         if (MODE == UG_UP) {
@@ -830,7 +837,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
         }
       }
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
-        if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+        if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
         goto done;
       }
       ptx::tc_fence_after();
@@ -931,6 +938,20 @@ done:
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  if (*aborted) {
+    // a wait gave up: every MMA this CTA issued completes (the MMA thread
+    // commits to a barrier of its own and waits for it) and the TMA loads
+    // already issued land (bounded waits) before the TMEM is freed
+    if (warp == 1 && lane == 0) {
+      ptx::tc_fence_after();
+      ptx::mma_commit(drain);
+      ptx::mbar_wait(drain, 0);
+    }
+    if (threadIdx.x == 0) ptx::spin_ns(100000);
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, 2 * UG_BN);

@@ -11,7 +11,10 @@
 // the bf16 hi and lo halves of an fp32 operand (v = hi + lo with |lo| <=
 // 2^-9 |v|, so hi*B + lo*B carries v*B with a relative error near 2^-17);
 // the row count may be a device value (number of overflow rows), in which
-// case row tiles past it are skipped by every role.
+// case row tiles past it are skipped by every role.  Every wait is bounded
+// (about a second); one that runs out sets TWELL_FLAG_TIMEOUT, and before the
+// CTA frees its TMEM and exits its MMAs complete (a commit waited for) and
+// its TMA loads land (a bounded 100 us wait).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -206,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // abort path: MMA drain
+  volatile uint32_t* aborted = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -254,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], 128);
     }
+    ptx::mbar_init(drain, 1);
+    *aborted = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hi = min(kb1 - seg_first, kb_seg[s]);
             for (int kb = lo; kb < hi; ++kb) {
               if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
-                if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+                { if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
                 goto done;
               }
               ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acc_phase = (local >> 1) & 1;
           ++local;
           if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
-            if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            { if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
             goto done;
           }
           ptx::tc_fence_after();
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool first = true;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!ptx::mbar_wait(&full[stage], phase)) {
-              if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+              { if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
               goto done;
             }
             ptx::tc_fence_after();
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc_phase = (local >> 1) & 1;
         ++local;
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
-          if (lane == 0 && p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          if (lane == 0) { if (p.status) atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
           goto done;
         }
         ptx::tc_fence_after();
@@ -376,6 +383,20 @@ done:
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  if (*aborted) {
+    // a wait gave up: every MMA this CTA issued completes (the MMA thread
+    // commits to a barrier of its own and waits for it) and the TMA loads
+    // already issued land (bounded waits) before the TMEM is freed
+    if (warp == 1 && lane == 0) {
+      ptx::tc_fence_after();
+      ptx::mma_commit(drain);
+      ptx::mbar_wait(drain, 0);
+    }
+    if (threadIdx.x == 0) ptx::spin_ns(100000);
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);

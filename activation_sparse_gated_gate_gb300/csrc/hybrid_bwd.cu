@@ -240,7 +240,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) ell_bwd_kernel(const BwdParams
           const uint32_t n_e = seq + e;
           const int s = static_cast<int>(n_e % static_cast<uint32_t>(P));
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bars[s], (n_e / P) & 1u))) {
-            if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            // wait (bounded) for this warp's row copies still in flight
+            // (entries e .. e + P - 1) before leaving
+            if (lane == 0) {
+              atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+              for (int r = e; r < min(m, e + P); ++r) {
+                const uint32_t n_r = seq + r;
+                if (!ptx::mbar_wait(&bars[n_r % static_cast<uint32_t>(P)], (n_r / P) & 1u)) break;
+              }
+            }
+            __syncwarp();
             return;
           }
           const BEntry en = list[e];

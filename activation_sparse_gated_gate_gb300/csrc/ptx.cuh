@@ -94,6 +94,14 @@ __device__ __forceinline__ bool mbar_wait_strict(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// Busy-wait for about `ns` nanoseconds (the drain of TMA loads whose
+// completion barrier can no longer complete after another role left).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
 // ---------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

@@ -29,7 +29,10 @@
 // accumulator once.
 //
 // Every wait is bounded (about a second); a wait that runs out sets
-// TWELL_FLAG_TIMEOUT and the CTA leaves its loops, frees its TMEM and exits.
+// TWELL_FLAG_TIMEOUT and the CTA leaves its loops; before it frees its TMEM
+// and exits, every MMA it issued completes (a commit to a barrier of its
+// own, waited for) and the TMA loads it issued land (a bounded 100 us wait:
+// their completion barrier may no longer complete once another role left).
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -105,6 +108,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
   uint64_t* raw_full = tempty + 2;
   uint64_t* raw_empty = raw_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + 4);
+  uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // abort path: MMA drain
+  volatile uint32_t* aborted = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -141,6 +146,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
       // ROWS: both expansion groups read each slot (one half of the tile each)
       ptx::mbar_init(&raw_empty[r], MODE == TC_ROWS ? 8 : 4);  // ROWS: the two groups of a tile
     }
+    ptx::mbar_init(drain, 1);
+    *aborted = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
         if (U.info(u, MODE, m_blk, n_blk, kb0, kb1) != 1) continue;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
-            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
             goto done;
           }
           uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
         const uint32_t acc_phase = (local >> 1) & 1;
         ++local;
         if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
-          atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+          { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
           goto done;
         }
         ptx::tc_fence_after();
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait(&full[stage], phase) ||
               (!Cfg::SAMPLE && !ptx::mbar_wait(&ready[stage], phase))) {
-            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
             goto done;
           }
           ptx::tc_fence_after();
@@ -250,7 +257,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
         // ROWS: one raw slot per tile (two K blocks); TRANS: one per K block
         for (int kb = kb0; kb < kb1; kb += (MODE == TC_ROWS ? 2 : 1)) {
           if (!ptx::mbar_wait(&raw_empty[slot], rphase ^ 1u)) {
-            atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+            { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
             goto done;
           }
           const int seg = kb / U.kb_per_seg;
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
                             ptx::mbar_wait(&raw_full[slot], rphase);
             if (MODE == TC_TRANS ? ptx::bar_any(bar_id, 128, !ok)
                                  : !__all_sync(0xffffffffu, ok)) {
-              if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+              if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
               goto done;
             }
             uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
       const uint32_t acc_phase = (local >> 1) & 1;
       ++local;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tfull[acc], acc_phase))) {
-        if (lane == 0) atomicOr(p.status, TWELL_FLAG_TIMEOUT);
+        if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
         goto done;
       }
       ptx::tc_fence_after();
@@ -546,6 +553,20 @@ done:
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  if (*aborted) {
+    // a wait gave up: every MMA this CTA issued completes (the MMA thread
+    // commits to a barrier of its own and waits for it) and the TMA loads
+    // already issued land (bounded waits) before the TMEM is freed
+    if (warp == 1 && lane == 0) {
+      ptx::tc_fence_after();
+      ptx::mma_commit(drain);
+      ptx::mbar_wait(drain, 0);
+    }
+    if (threadIdx.x == 0) ptx::spin_ns(100000);
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, 2 * BN);
