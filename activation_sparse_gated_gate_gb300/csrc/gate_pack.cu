@@ -10,10 +10,7 @@
 //               BK = 64 (128 B rows, 128B swizzle) into a STAGES-deep ring
 //   warp 1      TMEM allocator and MMA issuer (one thread): 128 x BN x 16
 //               bf16 MMAs accumulating fp32 in TMEM, two accumulator buffers
-//   warps 2..   epilogue: one set of four warps per TwELL tile of the
-//               accumulator (two sets for N = 256 tiles, so the packing of a
-//               tile's two column slices runs side by side and keeps up with
-//               the MMAs); each thread owns one output row of the 128-row
+//   warps 2..5  epilogue: each thread owns one output row of the 128-row
 //               tile, reads its 128 fp32 z of a slice from TMEM at once
 //               (four tcgen05.ld 32x32b), and packs the slice straight into
 //               TwELL: a 32-bit mask of z > 0 per 32-column chunk, a walk over
@@ -44,9 +41,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-// producer warp, MMA warp, then one set of four epilogue warps per 128
-// columns of the accumulator
-__host__ __device__ constexpr int threads_for(int BN) { return 64 + 128 * (BN / 128); }
+constexpr int kThreads = 192;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -75,8 +70,7 @@ struct GateCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SETS = BN / 128;      // epilogue warp sets
-  static constexpr int STAGING = 128 * 128 * SETS;  // a 32-column chunk per epilogue thread
+  static constexpr int STAGING = 128 * 128;  // a 32-column chunk per epilogue thread
   static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + BAR_BYTES + 1024;
 };
 
@@ -92,7 +86,7 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(threads_for(BN), 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gate_pack_kernel(const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_w, const GatePackParams p) {
   using Cfg = GateCfg<BN, STAGES>;
@@ -123,7 +117,7 @@ __global__ void __launch_bounds__(threads_for(BN), 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 128 * Cfg::SETS);
+      ptx::mbar_init(&tempty[a], 128);
     }
     ptx::mbar_init(drain, 1);
     *aborted = 0u;
@@ -211,7 +205,6 @@ __global__ void __launch_bounds__(threads_for(BN), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;       // row of the 128-row tile
-    const int set = (warp - 2) >> 2;     // the accumulator's 128-column slice of this set
     const int W = p.W;
     int local = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
@@ -230,11 +223,11 @@ __global__ void __launch_bounds__(threads_for(BN), 1)
       ptx::tc_fence_after();
       const int t = m_blk * BM + row;
       const bool valid = t < p.T;
-      uint8_t* my_stage = staging + (set * 128 + row) * 128;
+      uint8_t* my_stage = staging + row * 128;
 #pragma unroll 1
-      for (int sub = set; sub < set + 1; ++sub) {
+      for (int sub = 0; sub < BN / TWELL_TILE; ++sub) {
         const int kt = n_blk * (BN / TWELL_TILE) + sub;
-        if (kt >= p.n_t) break;  // uniform over the set
+        if (kt >= p.n_t) break;  // uniform over the CTA
         const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN + sub * TWELL_TILE) +
                                (static_cast<uint32_t>(q * 32) << 16);
         const size_t rt = static_cast<size_t>(valid ? t : 0) * p.n_t + kt;
@@ -369,7 +362,7 @@ twell_status launch(const DeviceInfo& dev, const CUtensorMap& mx, const CUtensor
       cudaSuccess)
     return TWELL_ERR_CUDA;
   const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
-  kern<<<grid, threads_for(BN), Cfg::SMEM, stream>>>(mx, mw, p);
+  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(mx, mw, p);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
