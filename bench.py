@@ -61,22 +61,22 @@ METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of ro
 TRAFFIC = {
     # 1.5B-class layer (profiles/ffn_fwd_tc_1.5B_T16384.md)
     ("twell_ffn_fwd_tc_sorted", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        730.17e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        728.36e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        789.17e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        789.81e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        776.32e6, "csrc/ffn_fwd.cu", "413694b7d064fc5c", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        775.73e6, "csrc/ffn_fwd.cu", "2ca95b29f788f850", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        149.88e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        149.71e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        211.39e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        212.57e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc_sorted", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        237.81e6, "csrc/ffn_tc.cu", "0c86577497c66b47", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        238.87e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        106.01e6, "csrc/ffn_fwd.cu", "413694b7d064fc5c", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        105.91e6, "csrc/ffn_fwd.cu", "2ca95b29f788f850", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        45.03e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        45.02e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
 
 
