@@ -13,28 +13,39 @@
 //   * the MMA is z^T = W_g^T x^T: M = 128 neurons (the W_g tile, K-major by
 //     TMA), N = the tokens rounded up to 16 (the x tile, rows past T read as
 //     zeros), fp32 accumulation in TMEM (lane = neuron, column = token);
-//   * each CTA walks its K blocks from a starting block that differs from
-//     tile to tile (and wraps around), so the loads in flight at any moment
-//     cover many column offsets of W_g instead of one 128-byte segment of
-//     rows exactly 2 D bytes apart, which kept the DRAM at a fifth of its
-//     bandwidth when every CTA walked K in step;
-//   * rank 1 reads its partial sums from TMEM into its (then idle) stage
-//     buffers as token rows; after a cluster barrier rank 0 adds them to its
-//     own through distributed shared memory, writes the sums as token rows
-//     of 128 values into its own stage buffers, and one epilogue thread per
-//     token packs its row into TwELL exactly as the batch kernel does
-//     (ascending slots, true count, fp32 spill slice when the count exceeds
-//     W); each word of the block bitmaps is one warp's ballot over its 32
-//     neurons, stored by that warp alone (so the bitmap needs no zeroing).
+//   * the producer issues the first round of stage fills right after it
+//     initialises the barriers, before the block-wide sync and the TMEM
+//     allocation;
+//   * the tokens are split between the two CTAs in 16-column chunks (rank 0
+//     the first half, rank 1 the rest): each CTA reads from TMEM the partial
+//     sums of the partner's tokens and stores them straight into the
+//     partner's exchange rows (one row of 128 fp32 per token, a region of
+//     its own, never a stage buffer) with remote shared-memory stores, and
+//     after one cluster barrier adds the partner's rows to its own partial
+//     sums;
+//   * packing is warp-parallel: two sets of four epilogue warps take
+//     alternate chunks of 16 tokens; for a chunk each warp of the set (32
+//     neurons, one per lane) takes one ballot per token, the set's four warps
+//     exchange the ballots through shared memory, and each active lane
+//     writes its value to slot (active neurons before it in the tile) when
+//     that is below W, so the slots hold the first W active columns in
+//     ascending order; the true count and, when it exceeds W, the ReLU'd
+//     fp32 slice in the spill list are written as by the batch kernel;
+//   * each block-bitmap word (one per 128-token block and 32 neurons) is the
+//     OR of the ballots of that quarter's warps (a shared-memory word each
+//     CTA clears in its prologue): rank 1 hands its part of block 0 to rank 0
+//     with a remote store, and each word is stored once (no zeroing).
 // Roles per CTA: warp 0 TMA producer, warp 1 TMEM allocation and MMA issue,
-// warps 2-5 epilogue (warp w reads TMEM lanes 32 (w mod 4) .. + 31).
+// warps 2-9 epilogue (warp w reads TMEM lanes 32 (w mod 4) .. + 31).
 //
 // Waits: every mbarrier wait is bounded (the call's bound, by default about
 // 1 s) and a CTA whose wait runs out sets TWELL_FLAG_TIMEOUT, drains the
-// TMA loads and MMAs it issued (waits of at most 1 s), skips its epilogue and
-// still reaches both cluster barriers, which every thread of both CTAs
-// passes on every path: the first publishes rank 1's partial sums, the
-// second keeps rank 1's shared memory alive until rank 0 has read it.
+// TMA loads and MMAs it issued (waits of at most 1 s), skips its epilogue,
+// tells the partner (which then skips its packing too) and still passes
+// every cluster barrier phase, which every thread of both CTAs reaches on
+// every path: the first (arrived at after the prologue, waited for before
+// the first remote store) guarantees the partner has started, the second
+// publishes the exchanged partial sums, the third the block-bitmap words.
 #include "common.cuh"
 #include "gate.cuh"
 #include "ptx.cuh"
@@ -44,11 +55,16 @@ namespace {
 
 constexpr int DM = 128;              // neurons per CTA tile = one TwELL tile
 constexpr int DK = 64;               // K block: 128-byte rows, 128B swizzle
-constexpr int kThreads = 192;        // producer, MMA issuer, four epilogue warps
+constexpr int kThreads = 320;        // producer, MMA issuer, two sets of four epilogue warps
 constexpr int kA = DM * DK * 2;      // W_g tile of a stage (16 KB)
 constexpr int kMaxStages = 8;
 constexpr int kRowBytes = DM * 4;    // one token's 128 fp32 values
-constexpr int kBarBytes = 256;
+// barrier area, byte offsets: full[8] 0, empty[8] 64, tfull 128, drain 136,
+// TMEM address 144, abort flag 148, partner's abort flag 152, rank 1's
+// block-0 words 160, this CTA's block words [2 blocks][4 quarters] 192,
+// ballots [2 sets][2][16 tokens][4 quarters] 256, spill slots [2 sets][2][16]
+// 1280
+constexpr int kBarBytes = 2048;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 struct DecParams {
@@ -57,6 +73,8 @@ struct DecParams {
   int32_t nkb;        // K blocks
   int32_t kb_split;   // first K block of rank 1
   int32_t stages, stage_bytes, region;  // region: bytes of the stage area
+  int32_t half;       // tokens of rank 0 (16-column chunks, rounded up); rank 1 has N - half
+  int32_t xch_bytes;  // exchange rows: half * 512
   uint32_t tmem_cols;
   float* val;
   uint8_t* col;
@@ -81,82 +99,25 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, uint64
                                     : ptx::mbar_wait_strict(bar, parity, limit_ns);
 }
 
-// Byte offset of neuron n in the staged row of token slot tl: 16-byte
-// chunks XOR-permuted by tl & 7, so one thread per row reading chunk c meets
-// fewer bank conflicts, and a warp writing consecutive neurons of one row
-// meets none.
-__device__ __forceinline__ uint32_t zoff(int tl, int n) {
-  return static_cast<uint32_t>(tl) * kRowBytes +
-         ((static_cast<uint32_t>((n >> 2) ^ (tl & 7)) << 4) | (static_cast<uint32_t>(n & 3) << 2));
-}
-
-// TwELL packing of token t's 128 gate values (staged row tl of zt) for
-// column tile `tile`: ascending active columns, the first W in the slots,
-// the true count, and the ReLU'd slice in the spill list when the count
-// exceeds W.
-__device__ __forceinline__ void pack_row(const DecParams& p, const uint8_t* zt, int tl, int t,
-                                         int tile) {
-  const uint8_t* row = zt + static_cast<size_t>(tl) * kRowBytes;
-  const size_t rt = static_cast<size_t>(t) * p.n_t + tile;
-  uint32_t mk[4] = {0u, 0u, 0u, 0u};
-  float* zd = p.z_debug ? p.z_debug + static_cast<size_t>(t) * p.F + tile * DM : nullptr;
-#pragma unroll
-  for (int c4 = 0; c4 < DM / 4; ++c4) {
-    const float4 v = *reinterpret_cast<const float4*>(row + ((c4 ^ (tl & 7)) << 4));
-    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (e[k] > 0.0f) mk[c4 >> 3] |= 1u << ((4 * c4 + k) & 31);
-    if (zd) reinterpret_cast<float4*>(zd)[c4] = v;
-  }
-  const int W = p.W;
-  float* vrow = p.val + rt * W;
-  uint8_t* crow = p.col + rt * W;
-  int c = 0;
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const uint32_t m = mk[ch];
-    if (m == 0u) continue;
-    uint32_t mm = m;
-    for (int e = c; e < W && mm != 0u; ++e) {
-      const int n = ch * 32 + __ffs(mm) - 1;
-      mm &= mm - 1u;
-      vrow[e] = *reinterpret_cast<const float*>(zt + zoff(tl, n));
-      crow[e] = static_cast<uint8_t>(n);
-    }
-    c += __popc(m);
-  }
-  p.cnt[rt] = static_cast<uint8_t>(c);
-  if (c > W) {
-    const int slot = atomicAdd(p.spill_n, 1);
-    p.spill_slot[rt] = slot;
-    if (slot < p.spill_cap) {
-      p.spill_rt[slot] = static_cast<int32_t>(rt);
-      float4* dst = reinterpret_cast<float4*>(p.spill_val + static_cast<size_t>(slot) * DM);
-#pragma unroll 8
-      for (int c4 = 0; c4 < DM / 4; ++c4) {
-        const float4 v = *reinterpret_cast<const float4*>(row + ((c4 ^ (tl & 7)) << 4));
-        dst[c4] = make_float4(v.x > 0.0f ? v.x : 0.0f, v.y > 0.0f ? v.y : 0.0f,
-                              v.z > 0.0f ? v.z : 0.0f, v.w > 0.0f ? v.w : 0.0f);
-      }
-    } else {
-      flag(p.status, TWELL_FLAG_SPILL_FULL);
-    }
-  }
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gate_decode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                        const __grid_constant__ CUtensorMap tmap_w, const DecParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* region = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(region + p.region);
+  uint8_t* xch = region + p.region;  // the partner's partial sums of this CTA's tokens
+  uint8_t* bars = xch + p.xch_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bars);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* drain = tfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile uint32_t* aborted = tmem_slot + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 144);
+  volatile uint32_t* aborted = reinterpret_cast<volatile uint32_t*>(bars + 148);
+  volatile uint32_t* peer_aborted = reinterpret_cast<volatile uint32_t*>(bars + 152);
+  uint32_t* bx = reinterpret_cast<uint32_t*>(bars + 160);
+  uint32_t* bacc = reinterpret_cast<uint32_t*>(bars + 192);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(bars + 256);
+  int32_t* sslot = reinterpret_cast<int32_t*>(bars + 1280);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -167,7 +128,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int rot = nloc > 0 ? (tile * 7 + static_cast<int>(rank) * 3) % nloc : 0;
   const int S = p.stages;
   uint32_t n_loads = 0;  // stage fills issued (producer thread)
+  int stage = 0;
+  uint32_t phase = 0;
 
+  auto fill = [&](int i) {
+    const int kb = kb0 + (i + rot < nloc ? i + rot : i + rot - nloc);
+    uint8_t* st = region + static_cast<size_t>(stage) * p.stage_bytes;
+    ptx::mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(p.stage_bytes));
+    ptx::tma_load_2d(st, &tmap_w, &full[stage], kb * DK, tile * DM);
+    ptx::tma_load_2d(st + kA, &tmap_x, &full[stage], kb * DK, 0);
+    ++n_loads;
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  };
+
+  const int first = nloc < S ? nloc : S;  // fills that need no free stage
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmap_x);
     ptx::prefetch_tmap(&tmap_w);
@@ -178,7 +155,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(tfull, 1);
     ptx::mbar_init(drain, 1);
     *aborted = 0u;
+    for (int i = 0; i < 8; ++i) bacc[i] = 0u;
     ptx::fence_mbar_init();
+    for (int i = 0; i < first; ++i) fill(i);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, p.tmem_cols);
@@ -187,57 +166,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // this CTA has started (waited for before the first remote store); no
+  // ordering: the partner writes only words this CTA never writes, and a
+  // releasing arrive would also wait for the fills issued above
+  ptx::cluster_arrive_relaxed();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int i = 0; i < nloc; ++i) {
-        const int kb = kb0 + (i + rot < nloc ? i + rot : i + rot - nloc);
+      for (int i = first; i < nloc; ++i) {
         if (!pipe_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
           flag(p.status, TWELL_FLAG_TIMEOUT);
           *aborted = 1u;
           break;
         }
-        uint8_t* st = region + static_cast<size_t>(stage) * p.stage_bytes;
-        ptx::mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(p.stage_bytes));
-        ptx::tma_load_2d(st, &tmap_w, &full[stage], kb * DK, tile * DM);
-        ptx::tma_load_2d(st + kA, &tmap_x, &full[stage], kb * DK, 0);
-        ++n_loads;
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        fill(i);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_bf16_f32(DM, p.N);
-      int stage = 0;
-      uint32_t phase = 0;
+      int st = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; i < nloc; ++i) {
-        if (!pipe_wait(&full[stage], phase, p.wait_ns)) {
+        if (!pipe_wait(&full[st], ph, p.wait_ns)) {
           flag(p.status, TWELL_FLAG_TIMEOUT);
           *aborted = 1u;
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_u32(region + static_cast<size_t>(stage) * p.stage_bytes);
+        const uint32_t a_addr = ptx::smem_u32(region + static_cast<size_t>(st) * p.stage_bytes);
         const uint32_t b_addr = a_addr + kA;
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk)
           ptx::mma_bf16(tmem_base, ptx::sdesc_kmajor_sw128(a_addr + kk * 32),
                         ptx::sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
                         (i > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(&empty[stage]);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
+        ptx::mma_commit(&empty[st]);
+        if (++st == S) {
+          st = 0;
+          ph ^= 1u;
         }
       }
       if (ok) ptx::mma_commit(tfull);
@@ -276,66 +248,131 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int q = warp & 3;           // TMEM lane quarter of this warp
   const int n = q * 32 + lane;      // neuron of the tile (epilogue threads)
   const bool epi = warp >= 2;
+  const int set = (warp - 2) >> 2;  // epilogue set: takes every other 16-token chunk
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-  if (epi && rank == 1 && !aborted_here) {
-    // partial sums as token rows (plain layout) in the idle stage buffers
-    ptx::tc_fence_after();
-    for (int c = 0; c < p.N; c += 16) {
-      uint32_t r[16];
-      ptx::tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(c), r);
-      ptx::tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        *reinterpret_cast<float*>(region + static_cast<size_t>(c + j) * kRowBytes + n * 4) =
-            __uint_as_float(r[j]);
-    }
-  }
-  ptx::tc_fence_before();
-  ptx::cluster_sync();  // rank 1's partial sums and abort flag are visible
+  const int own0 = rank == 0 ? 0 : p.half;     // this CTA's tokens: [own0, own1)
+  const int own1 = rank == 0 ? p.half : p.N;
+  const int oth0 = rank == 0 ? p.half : 0;     // the partner's
+  const int oth1 = rank == 0 ? p.N : p.half;
+  const uint32_t peer = rank ^ 1u;
 
-  if (epi && rank == 0) {
-    const uint32_t peer_aborted =
-        ptx::ld_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<uint32_t*>(aborted)), 1));
-    if (!aborted_here && peer_aborted == 0u) {
+  ptx::cluster_wait();  // the partner has started: its shared memory may be written
+  if (epi) {
+    if (!aborted_here) {
+      // the partner's tokens: partial sums into its exchange rows
       ptx::tc_fence_after();
-      const uint32_t part1 = ptx::mapa(ptx::smem_u32(region), 1);
-      uint8_t* zt = region;  // rank 0's own stage buffers are idle now
-      const int tl_own = (warp - 2) * 32 + lane;
-      for (int tb = 0; tb < p.N; tb += DM) {
-        const int nb = min(DM, p.N - tb);
-        bool any = false;
-        for (int c = tb; c < tb + nb; c += 16) {
-          // the partner's 16 partial sums first (one round trip for all),
-          // then this CTA's from TMEM
-          float pv[16];
+      const uint32_t rx = ptx::mapa(ptx::smem_u32(xch), peer) + static_cast<uint32_t>(n * 4);
+      for (int c = oth0 + 16 * set; c < oth1; c += 32) {
+        uint32_t r[16];
+        ptx::tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(c), r);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pv[j] = ptx::ld_cluster_f32(part1 + static_cast<uint32_t>((c + j) * kRowBytes + n * 4));
-          uint32_t r[16];
-          ptx::tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(c), r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = c + j;
-            const float v = __uint_as_float(r[j]) + pv[j];
-            *reinterpret_cast<float*>(zt + zoff(t - tb, n)) = v;
-            any |= t < p.T && v > 0.0f;
-          }
-        }
-        if (p.block_bits) {
-          // this warp alone produces the word: stored, not OR-ed (no zeroing)
-          const uint32_t word = __ballot_sync(0xffffffffu, any);
-          if (lane == 0)
-            p.block_bits[static_cast<size_t>(tb / DM) * (p.F / 32) + tile * 4 + q] = word;
-        }
-        ptx::bar_sync(1, 128);  // the block's rows are staged
-        const int t = tb + tl_own;
-        if (tl_own < nb && t < p.T) pack_row(p, zt, tl_own, t, tile);
-        ptx::bar_sync(1, 128);  // rows read before the next block overwrites them
+        for (int j = 0; j < 16; ++j)
+          ptx::st_cluster_u32(rx + static_cast<uint32_t>((c - oth0 + j) * kRowBytes), r[j]);
       }
     }
+    if (warp == 2 && lane == 0)
+      ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<uint32_t*>(peer_aborted)), peer),
+                          aborted_here ? 1u : 0u);
   }
-  ptx::cluster_sync();  // rank 1's shared memory stays until rank 0 has read it
+  ptx::tc_fence_before();
+  ptx::cluster_arrive();
+  ptx::cluster_wait();  // the partner's partial sums and abort flag are here
+
+  const bool go = !aborted_here && *peer_aborted == 0u;  // the same value in every thread
+  if (epi && go) {
+    ptx::tc_fence_after();
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t bar_id = 1u + static_cast<uint32_t>(set);
+    uint32_t bw0 = 0u, bw1 = 0u;  // this warp's block-bitmap words (blocks 0 and 1)
+    int par = 0;
+    for (int c = own0 + 16 * set; c < own1; c += 32, par ^= 1) {
+      uint32_t r[16];
+      ptx::tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(c), r);
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = *reinterpret_cast<const float*>(xch + (c - own0 + j) * kRowBytes + n * 4);
+      ptx::tmem_wait_ld();
+      uint32_t* mk = masks + (set * 2 + par) * 64;  // [token j][warp quarter]
+      int32_t* ss = sslot + (set * 2 + par) * 16;
+      uint32_t m[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        v[j] += __uint_as_float(r[j]);
+        m[j] = __ballot_sync(0xffffffffu, c + j < p.T && v[j] > 0.0f);
+        if (lane == j) mk[j * 4 + q] = m[j];
+        if (c + j < 128) bw0 |= m[j];
+        else bw1 |= m[j];
+      }
+      if (p.z_debug) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c + j < p.T) p.z_debug[static_cast<size_t>(c + j) * p.F + tile * DM + n] = v[j];
+      }
+      ptx::bar_sync(bar_id, 128);  // the four warps' ballots of these 16 tokens
+      // lane j < 16: token c + j's active count and the active neurons of
+      // the warps before this one
+      int cnt_j = 0, base_j = 0;
+      if (lane < 16) {
+        const uint4 w = *reinterpret_cast<const uint4*>(mk + lane * 4);
+        const int a0 = __popc(w.x), a1 = __popc(w.y), a2 = __popc(w.z), a3 = __popc(w.w);
+        cnt_j = a0 + a1 + a2 + a3;
+        base_j = (q > 0 ? a0 : 0) + (q > 1 ? a1 : 0) + (q > 2 ? a2 : 0);
+      }
+      const bool real = lane < 16 && c + lane < p.T;
+      const uint32_t spills = __ballot_sync(0xffffffffu, real && cnt_j > p.W);
+      if (q == 0 && real) {
+        const size_t rt = static_cast<size_t>(c + lane) * p.n_t + tile;
+        p.cnt[rt] = static_cast<uint8_t>(cnt_j);
+        if (cnt_j > p.W) {
+          const int slot = atomicAdd(p.spill_n, 1);
+          p.spill_slot[rt] = slot;
+          if (slot < p.spill_cap) p.spill_rt[slot] = static_cast<int32_t>(rt);
+          else flag(p.status, TWELL_FLAG_SPILL_FULL);
+          ss[lane] = slot;
+        }
+      }
+      int e[16];  // this lane's slot for each token (all shuffles issued together)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) e[j] = __shfl_sync(0xffffffffu, base_j, j) + __popc(m[j] & lt);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (((m[j] >> lane) & 1u) && e[j] < p.W) {
+          const size_t o = (static_cast<size_t>(c + j) * p.n_t + tile) * p.W + e[j];
+          p.val[o] = v[j];
+          p.col[o] = static_cast<uint8_t>(n);
+        }
+      }
+      if (spills != 0u) {
+        ptx::bar_sync(bar_id, 128);  // the spill slots of these tokens are published
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if ((spills >> j) & 1u) {
+            const int slot = ss[j];
+            if (slot < p.spill_cap)
+              p.spill_val[static_cast<size_t>(slot) * DM + n] = v[j] > 0.0f ? v[j] : 0.0f;
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      if (bw0 != 0u) atomicOr(&bacc[q], bw0);
+      if (bw1 != 0u) atomicOr(&bacc[4 + q], bw1);
+    }
+  }
+  // block words: rank 0's tokens all lie in block 0, rank 1's in block 0
+  // and / or block 1; rank 1's part of block 0 goes to rank 0
+  if (epi && rank == 1) {
+    ptx::bar_sync(3, 256);  // both sets' words are in bacc
+    if (set == 0 && lane == 0) ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(bx + q), 0), bacc[q]);
+  }
+  ptx::cluster_arrive();
+  ptx::cluster_wait();  // rank 1's words are here; neither CTA's memory is read afterwards
+  if (epi && set == 0 && go && lane == 0 && p.block_bits) {
+    if (rank == 0) p.block_bits[tile * 4 + q] = bacc[q] | bx[q];
+    else if (p.N > DM) p.block_bits[static_cast<size_t>(p.F / 32) + tile * 4 + q] = bacc[4 + q];
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, p.tmem_cols);
@@ -363,15 +400,15 @@ twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const 
   p.nkb = (D + DK - 1) / DK;
   p.kb_split = (p.nkb + 1) / 2;
   p.stage_bytes = kA + p.N * DK * 2;
+  p.half = (p.N / 16 + 1) / 2 * 16;
+  p.xch_bytes = p.half * kRowBytes;
   const int budget = (dev.max_smem_optin < 232448 ? dev.max_smem_optin : 232448) - 1024 -
-                     kBarBytes;
-  const int need_rows = (p.N > DM ? p.N : DM) * kRowBytes;  // exchange / staging rows
+                     kBarBytes - p.xch_bytes;
   int stages = budget / p.stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return TWELL_ERR_UNSUPPORTED;
   p.stages = stages;
-  p.region = stages * p.stage_bytes > need_rows ? stages * p.stage_bytes : need_rows;
-  if (p.region > budget) return TWELL_ERR_UNSUPPORTED;
+  p.region = stages * p.stage_bytes;
   p.tmem_cols = 32;
   while (p.tmem_cols < static_cast<uint32_t>(p.N)) p.tmem_cols <<= 1;
   p.val = out->val;
@@ -392,7 +429,7 @@ twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const 
   if ((st = make_tmap_bf16_2d(&mw, Wg_t, D, F, DK, DM)) != TWELL_OK) return st;
   if ((st = make_tmap_bf16_2d(&mx, x, D, T, DK, static_cast<uint32_t>(p.N))) != TWELL_OK)
     return st;
-  const int smem = p.region + kBarBytes + 1024;
+  const int smem = p.region + p.xch_bytes + kBarBytes + 1024;
   if (cudaFuncSetAttribute(gate_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return TWELL_ERR_CUDA;

@@ -366,6 +366,27 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for a barrier phase whose arrival and wait
+// are apart: arrive without ordering (only to learn later that every CTA of
+// the cluster has got there), arrive releasing this thread's earlier memory
+// accesses, and wait acquiring the other threads' released ones.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Store to another CTA's shared memory (a mapa address): issued without
+// waiting; ordered before the other CTA's reads by a release / acquire
+// cluster barrier phase.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Address of the same shared-memory variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
   uint32_t r;
