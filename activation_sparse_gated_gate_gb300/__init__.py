@@ -18,7 +18,7 @@ import os
 import torch
 
 __all__ = [
-    "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd",
+    "TwellError", "TwELL", "Hybrid", "lib", "twell_gate_pack", "twell_ffn_fwd", "twell_ffn_decode",
     "twell_ffn_fwd_tc", "twell_ffn_fwd_tc_sorted", "twell_to_f16",
     "twell_to_hybrid", "twell_workspace_size", "hybrid_ffn_fwd", "hybrid_ffn_fwd_noalloc",
     "hybrid_ffn_bwd", "hybrid_ffn_fwd_tc", "hybrid_ffn_bwd_tc",
@@ -77,6 +77,8 @@ _SIGNATURES = {
                                 c_ptr, c_ptr, c_ptr]),
     "twell_ffn_fwd": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_i32, c_ptr,
                               c_ptr, c_ptr]),
+    "twell_ffn_decode": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_i32,
+                                 ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_ptr, c_ptr]),
     "twell_ffn_fwd_tc": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_ptr, c_i32,
                                  c_ptr, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "twell_ffn_fwd_tc_sorted": (c_i32, [c_ptr, ctypes.POINTER(TwellStruct), c_ptr, c_ptr, c_ptr,
@@ -225,6 +227,32 @@ def twell_gate_pack(x, Wg_t, out: TwELL, z_debug=None, status=None, stream=None)
                                      _ptr(z_debug), _ptr(status), _stream(stream)),
                "twell_gate_pack")
     return out
+
+
+def twell_ffn_decode(x, Wg_t, Wu_t, Wd, out: TwELL, y=None, z_debug=None, status=None,
+                     stream=None):
+    """Decode-sized forward in one kernel (1 <= T <= 256): the gate with its
+    TwELL epilogue into ``out`` (as ``twell_gate_pack``) and the up + down
+    projection of every active entry into y; returns y [T][D] fp32
+    (allocated if not given, zeroed by the call)."""
+    for t, name in ((x, "x"), (Wg_t, "Wg_t"), (Wu_t, "Wu_t"), (Wd, "Wd")):
+        _need(t, torch.bfloat16, name)
+    T, D = x.shape
+    F = Wg_t.shape[0]
+    if Wg_t.shape[1] != D or Wu_t.shape != (F, D) or Wd.shape != (F, D):
+        raise ValueError("shape mismatch: x [T][D], Wg_t, Wu_t and Wd [F][D]")
+    if y is None:
+        y = torch.empty((T, D), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, "y")
+    if z_debug is not None:
+        _need(z_debug, torch.float32, "z_debug")
+    status = out.status if status is None else status
+    with torch.cuda.device(x.device):
+        _check(lib().twell_ffn_decode(_ptr(x), _ptr(Wg_t), _ptr(Wu_t), _ptr(Wd), T, D, F,
+                                      ctypes.byref(out.struct), _ptr(y), _ptr(z_debug),
+                                      _ptr(status), _stream(stream)),
+               "twell_ffn_decode")
+    return y
 
 
 def twell_gate_pack_wait_limit(ns: int) -> int:

@@ -46,6 +46,7 @@
 // every path: the first (arrived at after the prologue, waited for before
 // the first remote store) guarantees the partner has started, the second
 // publishes the exchanged partial sums, the third the block-bitmap words.
+#include "bounds.cuh"
 #include "common.cuh"
 #include "gate.cuh"
 #include "ptx.cuh"
@@ -62,9 +63,10 @@ constexpr int kRowBytes = DM * 4;    // one token's 128 fp32 values
 // barrier area, byte offsets: full[8] 0, empty[8] 64, tfull 128, drain 136,
 // TMEM address 144, abort flag 148, partner's abort flag 152, rank 1's
 // block-0 words 160, this CTA's block words [2 blocks][4 quarters] 192,
-// ballots [2 sets][2][16 tokens][4 quarters] 256, spill slots [2 sets][2][16]
-// 1280
+// entry count 224, ballots [2 sets][2][16 tokens][4 quarters] 256, spill
+// slots [2 sets][2][16] 1280
 constexpr int kBarBytes = 2048;
+constexpr int kEntryBytes = 8;       // (token * 128 + neuron, gate value) of an active entry
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 struct DecParams {
@@ -88,6 +90,11 @@ struct DecParams {
   float* z_debug;
   int32_t* status;
   uint64_t wait_ns;
+  // fused up + down projection (twell_ffn_decode); y NULL skips it
+  const uint16_t* x;
+  const uint16_t* Wu_t;
+  const uint16_t* Wd;
+  float* y;
 };
 
 __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
@@ -97,6 +104,28 @@ __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
 __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   return limit_ns >= kDefaultWaitNs ? ptx::mbar_wait(bar, parity, limit_ns)
                                     : ptx::mbar_wait_strict(bar, parity, limit_ns);
+}
+
+// The eight bf16 of a 16-byte chunk as fp32 (exact: a bf16 is the top half
+// of its fp32).
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* f) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(u[k] << 16);
+    f[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+  }
+}
+
+// Sum of the eight products of two 16-byte bf16 chunks, in fp32 (in order).
+__device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b) {
+  float fa[8], fb[8];
+  bf16x8_to_f32(a, fa);
+  bf16x8_to_f32(b, fb);
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s = fmaf(fa[k], fb[k], s);
+  return s;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -116,6 +145,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile uint32_t* peer_aborted = reinterpret_cast<volatile uint32_t*>(bars + 152);
   uint32_t* bx = reinterpret_cast<uint32_t*>(bars + 160);
   uint32_t* bacc = reinterpret_cast<uint32_t*>(bars + 192);
+  int32_t* n_ent = reinterpret_cast<int32_t*>(bars + 224);
+  // active entries of this CTA's tokens (fused projection), in the stage
+  // buffers once the MMAs are done
+  uint2* ent = reinterpret_cast<uint2*>(region);
   uint32_t* masks = reinterpret_cast<uint32_t*>(bars + 256);
   int32_t* sslot = reinterpret_cast<int32_t*>(bars + 1280);
 
@@ -156,6 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(drain, 1);
     *aborted = 0u;
     for (int i = 0; i < 8; ++i) bacc[i] = 0u;
+    *n_ent = 0;
     ptx::fence_mbar_init();
     for (int i = 0; i < first; ++i) fill(i);
   }
@@ -344,6 +378,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           p.col[o] = static_cast<uint8_t>(n);
         }
       }
+      if (p.y) {
+        // every active entry of the chunk (slots and spill alike) into the
+        // CTA's list, and its neuron's W_u and W_d rows on their way to L2
+        int pre[16], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pre[j] = tot;
+          tot += __popc(m[j]);
+        }
+        if (tot > 0) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(n_ent, tot);
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const size_t roff = (static_cast<size_t>(tile) * DM + n) * p.D;
+          bool mine = false;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if ((m[j] >> lane) & 1u) {
+              const int idx = base + pre[j] + __popc(m[j] & lt);
+              if (in_bounds(idx, (own1 - own0) * DM, p.status))
+                ent[idx] = make_uint2(static_cast<uint32_t>((c + j) * DM + n), __float_as_uint(v[j]));
+              mine = true;
+            }
+          }
+          if (mine) {
+            ptx::prefetch_l2_bulk(p.Wu_t + roff, static_cast<uint32_t>(p.D) * 2u);
+            ptx::prefetch_l2_bulk(p.Wd + roff, static_cast<uint32_t>(p.D) * 2u);
+          }
+        }
+      }
       if (spills != 0u) {
         ptx::bar_sync(bar_id, 128);  // the spill slots of these tokens are published
 #pragma unroll
@@ -361,12 +425,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (bw1 != 0u) atomicOr(&bacc[4 + q], bw1);
     }
   }
+  if (epi) ptx::bar_sync(3, 256);  // both sets' block words and entries are in
+  if (epi && go && p.y) {
+    // fused projection: each epilogue warp takes whole entries in turn;
+    // u = x_t . W_u[:, j] over 16-byte chunks of the rows (lane-strided),
+    // reduced across the warp, then y_t += (h u) W_d[j, :] with float4
+    // atomics (y zeroed by the call)
+    const int nE = *n_ent;
+    const int nq = p.D / 8;
+    const uint4* x4 = reinterpret_cast<const uint4*>(p.x);
+    const uint4* wu4 = reinterpret_cast<const uint4*>(p.Wu_t);
+    const uint4* wd4 = reinterpret_cast<const uint4*>(p.Wd);
+    for (int ei = warp - 2; ei < nE; ei += 8) {
+      const uint2 en = ent[ei];
+      const int t = static_cast<int>(en.x / DM);
+      const size_t j = static_cast<size_t>(tile) * DM + en.x % DM;
+      const uint4* xr = x4 + static_cast<size_t>(t) * nq;
+      const uint4* ur = wu4 + j * nq;
+      const uint4* dr = wd4 + j * nq;
+      float u = 0.0f;
+      for (int q0 = 0; q0 < nq; q0 += 256) {
+        uint4 xa[8], wa[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = q0 + 32 * i + lane;
+          if (q < nq) {
+            xa[i] = __ldg(xr + q);
+            wa[i] = __ldg(ur + q);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (q0 + 32 * i + lane < nq) u += dot8_bf16(xa[i], wa[i]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+      const float a = __uint_as_float(en.y) * u;
+      float* yr = p.y + static_cast<size_t>(t) * p.D;
+      for (int q0 = 0; q0 < nq; q0 += 256) {
+        uint4 wa[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = q0 + 32 * i + lane;
+          if (q < nq) wa[i] = __ldg(dr + q);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = q0 + 32 * i + lane;
+          if (q < nq) {
+            float f[8];
+            bf16x8_to_f32(wa[i], f);
+            float4* o = reinterpret_cast<float4*>(yr + 8 * q);
+            atomicAdd(o, make_float4(a * f[0], a * f[1], a * f[2], a * f[3]));
+            atomicAdd(o + 1, make_float4(a * f[4], a * f[5], a * f[6], a * f[7]));
+          }
+        }
+      }
+    }
+  }
   // block words: rank 0's tokens all lie in block 0, rank 1's in block 0
   // and / or block 1; rank 1's part of block 0 goes to rank 0
-  if (epi && rank == 1) {
-    ptx::bar_sync(3, 256);  // both sets' words are in bacc
-    if (set == 0 && lane == 0) ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(bx + q), 0), bacc[q]);
-  }
+  if (epi && rank == 1 && set == 0 && lane == 0)
+    ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(bx + q), 0), bacc[q]);
   ptx::cluster_arrive();
   ptx::cluster_wait();  // rank 1's words are here; neither CTA's memory is read afterwards
   if (epi && set == 0 && go && lane == 0 && p.block_bits) {
@@ -388,7 +508,7 @@ bool gate_decode_supported(int32_t T, int32_t D) {
 twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const uint16_t* Wg_t,
                                 int32_t T, int32_t D, int32_t F, const twell_t* out,
                                 float* z_debug, int32_t* status_dev, uint64_t wait_ns,
-                                cudaStream_t s) {
+                                const DecodeFfn* ffn, cudaStream_t s) {
   if (!gate_decode_supported(T, D)) return TWELL_ERR_UNSUPPORTED;
   DecParams p;
   p.T = T;
@@ -409,6 +529,9 @@ twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const 
   if (stages < 2) return TWELL_ERR_UNSUPPORTED;
   p.stages = stages;
   p.region = stages * p.stage_bytes;
+  // the entry list of the fused projection: at most every neuron of every
+  // token of rank 0 (the larger half)
+  if (ffn && p.region < p.half * DM * kEntryBytes) return TWELL_ERR_UNSUPPORTED;
   p.tmem_cols = 32;
   while (p.tmem_cols < static_cast<uint32_t>(p.N)) p.tmem_cols <<= 1;
   p.val = out->val;
@@ -423,6 +546,10 @@ twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const 
   p.z_debug = z_debug;
   p.status = status_dev;
   p.wait_ns = wait_ns;
+  p.x = x;
+  p.Wu_t = ffn ? ffn->Wu_t : nullptr;
+  p.Wd = ffn ? ffn->Wd : nullptr;
+  p.y = ffn ? ffn->y : nullptr;
 
   CUtensorMap mx, mw;
   twell_status st;

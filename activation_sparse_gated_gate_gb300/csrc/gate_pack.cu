@@ -410,7 +410,8 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
   // (every TwELL tile on a 2-CTA cluster, W_g streamed once; it stores every
   // block-bitmap word itself).
   if (gate_decode_supported(T, D))
-    return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, p.wait_ns, s);
+    return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, p.wait_ns,
+                              nullptr, s);
 
   if (out->block_bits &&
       cudaMemsetAsync(out->block_bits, 0,
@@ -430,6 +431,31 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
   if ((st = make_tmap_bf16_2d(&mx, x, D, T, BK, BM)) != TWELL_OK) return st;
   if ((st = make_tmap_bf16_2d(&mw, Wg_t, D, F, BK, BN)) != TWELL_OK) return st;
   return wide ? launch<256, 4>(dev, mx, mw, p, s) : launch<128, 6>(dev, mx, mw, p, s);
+}
+
+extern "C" twell_status twell_ffn_decode(const uint16_t* x, const uint16_t* Wg_t,
+                                         const uint16_t* Wu_t, const uint16_t* Wd, int32_t T,
+                                         int32_t D, int32_t F, const twell_t* out, float* y,
+                                         float* z_debug, int32_t* status_dev, void* stream) {
+  using namespace twell;
+  if (T < 0 || D <= 0 || F <= 0 || D % 8 != 0 || F % TWELL_TILE != 0) return TWELL_ERR_INVALID;
+  twell_status st = check_twell(out, T, F, true);
+  if (st != TWELL_OK) return st;
+  if (T == 0) return TWELL_OK;
+  if (!x || !Wg_t || !Wu_t || !Wd || !y) return TWELL_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(Wg_t) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y))
+    return TWELL_ERR_INVALID;
+  if (z_debug && !aligned16(z_debug)) return TWELL_ERR_INVALID;
+  if (!gate_decode_supported(T, D)) return TWELL_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if ((st = require_sm103(&dev)) != TWELL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(out->spill_n, 0, sizeof(int32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
+  if (cudaMemsetAsync(y, 0, static_cast<size_t>(T) * D * sizeof(float), s) != cudaSuccess)
+    return TWELL_ERR_CUDA;
+  const DecodeFfn ffn{Wu_t, Wd, y};
+  return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev,
+                            g_wait_ns.load(std::memory_order_relaxed), &ffn, s);
 }
 
 extern "C" uint64_t twell_gate_pack_wait_limit(uint64_t ns) {

@@ -104,6 +104,14 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 
 // ---------------------------------------------------------------------- TMA
 
+// Bring `bytes` (a multiple of 16) of global memory at a 16-byte aligned
+// address into L2, asynchronously (no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -468,6 +468,33 @@ def updown_roofline(T, D, F, nnz, n_active, ms, hbm_gbs, fma_tflops, bf16_tflops
     return out
 
 
+def decode_roofline(T, D, F, nnz, n_active, ms, hbm_gbs, fma_tflops, bf16_tflops):
+    """The one-kernel decode forward (twell_ffn_decode: gate, TwELL and the
+    up + down projection) against the method's work: bytes = x in (bf16),
+    W_g, the W_u and W_d rows of every neuron active in some row, y out
+    (fp32) and the TwELL written; flops = 2 T D F for the gate (tensor
+    cores) and 4 D per active entry (FP32 FMA pipe); binding = the longest
+    of the three roofline times."""
+    nbytes = (2.0 * T * D + 2.0 * F * D + 4.0 * n_active * D + 4.0 * T * D + 5.0 * nnz
+              + T * (F // 128))
+    flops = 4.0 * D * nnz
+    tflops = 2.0 * T * D * F
+    t = ms * 1e-3
+    times = {"hbm": nbytes / (hbm_gbs * 1e9), "alu": flops / (fma_tflops * 1e12),
+             "tensor": tflops / (bf16_tflops * 1e12)}
+    out = {"bytes": nbytes, "flops": flops, "tensor_flops": tflops, "ms": ms,
+           "hbm": {"achieved_gbs": nbytes / t / 1e9, "peak": hbm_gbs,
+                   "frac": times["hbm"] / t, "t_us": times["hbm"] * 1e6},
+           "alu": {"achieved_tflops": flops / t / 1e12, "peak": fma_tflops,
+                   "frac": times["alu"] / t, "t_us": times["alu"] * 1e6},
+           "tensor": {"achieved_tflops": tflops / t / 1e12, "peak": bf16_tflops,
+                      "frac": times["tensor"] / t, "t_us": times["tensor"] * 1e6}}
+    b = max(times, key=times.get)
+    out["bound"] = b
+    out["binding"] = {"bound": b, "t_us": times[b] * 1e6, "frac": times[b] / t}
+    return out
+
+
 def train_rooflines(D, F, T, nnz_ell, n_dense, nnz_total, kernels_ms, hbm_gbs, fma_tflops,
                     bf16_tflops):
     """Per-kernel rooflines of the training step (method's work).
@@ -613,6 +640,11 @@ class InferCase:
         # the tensor-core forward's down GEMM takes W_d in fp16: converted once
         # per model, like any weight preparation, outside the timed steps
         self.Wd16 = tw.twell_to_f16(self.Wd)
+        # decode batches: the one-kernel forward (its own TwELL and y)
+        self.dec = w.T <= 256 and w.D > 64
+        if self.dec:
+            self.h_dec = tw.TwELL(w.T, w.F, w.width, device=dev)
+            self.y_dec = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
 
     def gate(self, stream=None):
         import activation_sparse_gated_gate_gb300 as tw
@@ -637,6 +669,11 @@ class InferCase:
     def fwd(self, kind, stream=None):
         {"tc": self.fwd_tc, "tcs": self.fwd_tcs, "cc": self.fwd_cc}[kind](stream)
 
+    def step_dec(self, stream=None):
+        import activation_sparse_gated_gate_gb300 as tw
+        tw.twell_ffn_decode(self.x, self.Wg, self.Wu, self.Wd, self.h_dec, y=self.y_dec,
+                            stream=stream or self.stream)
+
     def active_union(self):
         """Neurons active in some row (one untimed pack with z exported)."""
         import torch
@@ -648,14 +685,23 @@ class InferCase:
         return n
 
 
-FWD_NAMES = {"tc": "twell_ffn_fwd_tc", "tcs": "twell_ffn_fwd_tc_sorted", "cc": "twell_ffn_fwd"}
+FWD_NAMES = {"tc": "twell_ffn_fwd_tc", "tcs": "twell_ffn_fwd_tc_sorted", "cc": "twell_ffn_fwd",
+             "dec": "twell_ffn_decode"}
 # kernels of the library launched by one forward call: union scan + up +
 # down GEMMs; the sorted variant adds three sort kernels, the x copy and the
-# union bitmaps; the CUDA-core forward is one kernel (the gate is one more)
-FWD_LAUNCHES = {"tc": 3, "tcs": 8, "cc": 1}
-# per timed iteration of infer_entry: the gate graph, each forward's graph
-# and each step's graph (gate + forward)
-ITER_LAUNCHES = 1 + sum(FWD_LAUNCHES.values()) + sum(1 + n for n in FWD_LAUNCHES.values())
+# union bitmaps; the CUDA-core forward is one kernel (the gate is one more);
+# the one-kernel decode forward includes the gate
+FWD_LAUNCHES = {"tc": 3, "tcs": 8, "cc": 1, "dec": 1}
+
+
+def iter_launches(kinds):
+    """Library kernels per timed iteration of infer_entry: the gate graph,
+    each forward's graph and each step's graph (gate + forward; the decode
+    forward's step is its one kernel)."""
+    n = 1
+    for kd in kinds:
+        n += FWD_LAUNCHES[kd] if kd == "dec" else 1 + 2 * FWD_LAUNCHES[kd]
+    return n
 
 
 def _capture(dev, fn):
@@ -688,21 +734,26 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
     w = case.w
     stream = case.stream
     hbm, bf16, _, src = peaks
-    kinds = ("tc", "tcs", "cc")
+    kinds = ("tc", "tcs", "cc") + (("dec",) if case.dec else ())
     n_active = case.active_union()
     graphs = {"gate": _capture(case.dev, lambda st: case.gate(st))}
     for kd in kinds:
+        if kd == "dec":
+            graphs["step_dec"] = _capture(case.dev, lambda st: case.step_dec(st))
+            continue
         graphs[kd] = _capture(case.dev, lambda st, kd=kd: case.fwd(kd, st))
         graphs["step_" + kd] = _capture(case.dev,
                                         lambda st, kd=kd: (case.gate(st), case.fwd(kd, st)))
-    order = ["gate"] + [k for kd in kinds for k in (kd, "step_" + kd)]
+    order = ["gate"] + [k for kd in kinds
+                        for k in (("step_dec",) if kd == "dec" else (kd, "step_" + kd))]
     for _ in range(warmup):
         for name in order:
             flush.zero_()
             graphs[name].replay()
     torch.cuda.synchronize()
-    if int(case.h.status.item()) != 0:
-        raise RuntimeError(f"device status flags {int(case.h.status.item())} ({w.name})")
+    for hh in (case.h, case.h_dec) if case.dec else (case.h,):
+        if int(hh.status.item()) != 0:
+            raise RuntimeError(f"device status flags {int(hh.status.item())} ({w.name})")
     K = steps
     ev = {name: [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
           for name in order}
@@ -714,13 +765,19 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
             graphs[name].replay()
             e[1].record(stream)
     torch.cuda.synchronize()
-    if int(case.h.status.item()) != 0:
-        raise RuntimeError(f"device status flags {int(case.h.status.item())} ({w.name})")
+    for hh in (case.h, case.h_dec) if case.dec else (case.h,):
+        if int(hh.status.item()) != 0:
+            raise RuntimeError(f"device status flags {int(hh.status.item())} ({w.name})")
     t = {name: statistics.mean(ev[name][i][0].elapsed_time(ev[name][i][1]) for i in range(K))
          for name in order}
     step = {kd: max_over_ranks(t["step_" + kd], case.dev) for kd in kinds}
+    if forward == "dec" and not case.dec:
+        forward = "auto"  # the one-kernel forward exists for decode batches only
+    if forward not in ("auto",) + kinds:
+        raise RuntimeError(f"--forward {forward}: not available for {w.name}")
     best = min(step, key=step.get) if forward == "auto" else forward
-    for kd, yk in (("tc", case.y), ("tcs", case.y_tcs)):
+    checks = [("tc", case.y), ("tcs", case.y_tcs)] + ([("dec", case.y_dec)] if case.dec else [])
+    for kd, yk in checks:
         rel = float((yk - case.y_cc).norm() / max(float(case.y_cc.norm()), 1e-30))
         if not rel < 5e-3:
             raise RuntimeError(f"{FWD_NAMES[kd]} and the CUDA-core forward differ (relative "
@@ -732,6 +789,10 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
     ws_n = int(os.environ.get("WORLD_SIZE", "1"))
     kernels = {"twell_gate_pack": gate_roofline(w.T, w.D, w.F, nnz, g_ms, hbm, bf16)}
     for kd in kinds:
+        if kd == "dec":
+            kernels[FWD_NAMES[kd]] = decode_roofline(w.T, w.D, w.F, nnz, n_active,
+                                                     t["step_dec"], hbm, fma, bf16)
+            continue
         kernels[FWD_NAMES[kd]] = updown_roofline(
             w.T, w.D, w.F, nnz, n_active, t[kd], hbm, fma, bf16,
             union_sum if kd == "tc" else None)
@@ -746,7 +807,9 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
         "timing": ("each call and each step captured as a CUDA graph, replayed after an L2 "
                    "flush between CUDA events; mean of K"),
     }
-    return entry, {"use": best, "fwd_ms": t[best], "gate_ms": g_ms,
+    entry["launches_per_iteration"] = iter_launches(kinds)
+    fwd_ms = t["step_dec"] if best == "dec" else t[best]
+    return entry, {"use": best, "fwd_ms": fwd_ms, "gate_ms": 0.0 if best == "dec" else g_ms,
                    "fwd_name": FWD_NAMES[best], "nnz": nnz, "n_active": n_active,
                    "union_sum": union_sum}
 
@@ -773,6 +836,24 @@ def headline_roofline(entry, raw, peaks, fma_meta):
     name = raw["fwd_name"]
     r = k[name]
     tr, prof = _traffic(name, entry["workload"])
+    if name == "twell_ffn_decode":
+        b = r["binding"]["bound"]
+        unit = "GB/s" if b == "hbm" else "TFLOP/s"
+        ach = r["hbm"]["achieved_gbs"] if b == "hbm" else (
+            r["alu"]["achieved_tflops"] if b == "alu" else r["tensor"]["achieved_tflops"])
+        return {"kernel": name, "bound": b, "achieved": ach, "peak": r[b]["peak"], "unit": unit,
+                "frac": r["binding"]["frac"],
+                "peak_source": {"hbm": f"{src} HBM copy", "alu": "measured FFMA (twell_probe_fma)",
+                                "tensor": f"{src} bf16 burst"}[b],
+                "traffic": tr, "traffic_source": prof,
+                "work": ("the whole decode step in one kernel: bytes = x in + W_g + W_u/W_d rows "
+                         "of every active neuron + y out (fp32) + TwELL written; flops = 2 T D F "
+                         "(gate, tensor cores) and 4 D per active entry (FP32 FMA); binding = "
+                         "the longest of the three times"),
+                "algorithmic_bytes": r["bytes"], "algorithmic_flops": r["flops"],
+                "hbm": {"achieved": r["hbm"]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
+                        "frac": r["hbm"]["frac"], "peak_source": f"{src} HBM copy"},
+                "binding": r["binding"]}
     out = {"kernel": name, "bound": r["bound"]}
     if r["bound"] == "alu":
         out.update({"achieved": r["alu"]["achieved_tflops"], "peak": r["alu"]["peak"],
@@ -1101,7 +1182,7 @@ def e2e_pipeline(args, case, flush, K):
         return chunk_state[key]
 
     def kind_for(n):
-        if args.forward != "auto":
+        if args.forward not in ("auto", "dec"):
             return args.forward
         return min(("tc", "tcs", "cc"), key=lambda kd: chunk_ms(n, kd))
 
@@ -1212,7 +1293,8 @@ def run_ours(args, head_cfg):
     e2e = None if args.no_e2e else e2e_pipeline(args, case, flush, K)
     energy = None
     if not args.no_energy:
-        step = lambda: (case.gate(), case.fwd(raw["use"]))
+        step = ((lambda: case.step_dec()) if raw["use"] == "dec"
+                else (lambda: (case.gate(), case.fwd(raw["use"]))))
         e_ours = energy_per_token(step, w.T, stream, local)
         e_dense = energy_per_token(
             lambda: (torch.relu(case.x @ case.Wg.t()) * (case.x @ case.Wu.t())) @ case.Wd,
@@ -1244,7 +1326,7 @@ def run_ours(args, head_cfg):
 
     value = entry["tokens_per_s"]
     ms_step = entry["ms_per_step"]
-    use_tc = raw["use"] != "cc"
+    use_tc = raw["use"] in ("tc", "tcs")
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -1264,13 +1346,13 @@ def run_ours(args, head_cfg):
         "e2e": e2e,
         # our kernels in the headline's timed region: every iteration replays
         # the gate, each forward and each step once
-        "gpu_launches": K * ITER_LAUNCHES,
+        "gpu_launches": K * entry["launches_per_iteration"],
         "roofline": roof,
         "headline": entry,
         "configs": configs,
         "fma_peak": fma_meta,
         "forward": raw["fwd_name"],
-        "forward_choice": ("the fastest of the three measured steps" if args.forward == "auto"
+        "forward_choice": ("the fastest of the measured steps" if args.forward == "auto"
                            else f"fixed by --forward {args.forward}"),
         "energy": energy,
         "clocks": clk_sum,
@@ -1309,7 +1391,7 @@ def main():
     ap.add_argument("--train-steps", type=int, default=5)
     ap.add_argument("--no-energy", action="store_true", help="skip the energy-per-token section")
     ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack section")
-    ap.add_argument("--forward", default="auto", choices=["auto", "tc", "tcs", "cc"],
+    ap.add_argument("--forward", default="auto", choices=["auto", "tc", "tcs", "cc", "dec"],
                     help="inference forward of the steps and the end-to-end pipeline: the "
                          "faster measured one (auto) or a fixed one (profiling runs, where a "
                          "profiler's per-launch overhead distorts the comparison)")

@@ -132,6 +132,25 @@ twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T,
                              int32_t* status_dev, void* stream);
 
 /*
+ * Decode-sized forward in one kernel (paper sections 2.B.1 and 2.B.2
+ * together): the gate GEMM z = x W_g with its TwELL epilogue, exactly as
+ * twell_gate_pack (same `out`, same z_debug), and in the same kernel, for
+ * every active entry (t, j) of z -- slots and spill alike, so nothing is
+ * dropped when the spill list is full -- u = x_t . W_u[:, j] (fp32) and
+ * y_t += (h u) W_d[j, :] with fp32 atomics.  Rows with no active entry get
+ * y_t = 0.
+ *   x   [T][D] bf16   Wg_t, Wu_t, Wd  [F][D] bf16   y  [T][D] fp32 (written;
+ *   zeroed by the call, stream-ordered)
+ * Supports 1 <= T <= 256 with D > 64 (TWELL_ERR_UNSUPPORTED otherwise:
+ * use twell_gate_pack + twell_ffn_fwd); D % 8 == 0, all pointers 16-byte
+ * aligned.  Repeats agree to fp32 rounding, not bit for bit (atomics).
+ */
+twell_status twell_ffn_decode(const uint16_t* x, const uint16_t* Wg_t, const uint16_t* Wu_t,
+                              const uint16_t* Wd, int32_t T, int32_t D, int32_t F,
+                              const twell_t* out, float* y, float* z_debug, int32_t* status_dev,
+                              void* stream);
+
+/*
  * Bound, in nanoseconds, on each pipeline wait of the gate kernel launched
  * by later twell_gate_pack calls (process-wide; 0 restores the default of
  * 1e9 ns); returns the previous bound.  A wait that runs out sets

@@ -54,3 +54,23 @@ def test_train_rooflines_count_sparse_and_dense_work():
     t = b["t_alu_us"] + b["t_tensor_us"]
     assert b["frac"] == pytest.approx(max(t, b["t_hbm_us"]) / 5200)
     assert r["twell_gate_pack"]["bound"] == "tensor"
+
+
+def test_decode_roofline_counts_the_whole_step_once():
+    # T=64 tokens of the decode layer (d_model 2048, d_ff 8192), 2600 active
+    # entries over 2245 neurons: x in, W_g, the active neurons' W_u/W_d rows,
+    # y out (fp32) and the TwELL written; HBM binds at this size
+    T, D, F, nnz, na = 64, 2048, 8192, 2600, 2245
+    r = bench.decode_roofline(T, D, F, nnz, na, 0.020, 6784.5, 80.0, 1906.6)
+    nbytes = 2 * T * D + 2 * F * D + 4 * na * D + 4 * T * D + 5 * nnz + T * (F // 128)
+    assert r["bytes"] == nbytes
+    assert r["bound"] == "hbm"
+    assert r["binding"]["frac"] == pytest.approx(nbytes / 6784.5e9 / 20e-6)
+    assert r["tensor"]["frac"] == pytest.approx(2 * T * D * F / 1906.6e12 / 20e-6)
+    assert r["alu"]["frac"] == pytest.approx(4 * D * nnz / 80e12 / 20e-6)
+
+
+def test_iter_launches():
+    # gate + (forward + step) for the three batch forwards: 1 + (3+4) + (8+9) + (1+2)
+    assert bench.iter_launches(("tc", "tcs", "cc")) == 28
+    assert bench.iter_launches(("tc", "tcs", "cc", "dec")) == 29

@@ -5,7 +5,8 @@ bounds, spill slots, row maps, per-neuron record offsets, union positions)
 is range-checked and an index outside its buffer sets TWELL_FLAG_BOUNDS
 instead of being used.  This stands in for a memory checker on this pool.
 
-The small parity cases of the inference and training paths run through that
+The small parity cases of the inference and training paths (the one-kernel
+decode forward among them) run through that
 build: no index falls outside its buffer (the flag stays clear) and every
 result equals the normal build's (bit for bit where the kernels are
 deterministic, to fp32 rounding where they add with atomics).  One TwELL
@@ -40,8 +41,14 @@ def _inference(w, d, spill_cap=None):
     tc = w.D % 64 == 0
     y_tc = tw.twell_ffn_fwd_tc(d["x"], h, d["Wu_t"], d["Wd"]) if tc else y
     y_tcs = tw.twell_ffn_fwd_tc_sorted(d["x"], h, d["Wu_t"], d["Wd"]) if tc else y
+    # the one-kernel decode forward (decode batches; its own TwELL)
+    dec = w.T <= 256 and w.D > 64
+    hd = tw.TwELL(w.T, w.F, w.width, spill_cap=spill_cap)
+    y_dec = tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], hd) if dec else y
     torch.cuda.synchronize()
-    return h, z, y, (y_tc, y_tcs)
+    if dec:
+        assert int(hd.status.item()) & tw.FLAG_BOUNDS == 0
+    return h, z, y, (y_tc, y_tcs), y_dec
 
 
 def _slots(h):
@@ -60,10 +67,10 @@ def _slots(h):
 def test_inference_under_bounds_checks(T, D, F, p, W, cap):
     w = workloads.random_small(T, D, F, p, W, seed=T + 7)
     d = upload(w)
-    h0, z0, y0, yt0 = _inference(w, d, cap)
+    h0, z0, y0, yt0, yd0 = _inference(w, d, cap)
     s0 = int(h0.status.item())
     with tw.library(tw.BOUNDS_LIB_PATH):
-        h1, z1, y1, yt1 = _inference(w, d, cap)
+        h1, z1, y1, yt1, yd1 = _inference(w, d, cap)
     s1 = int(h1.status.item())
     assert s1 & tw.FLAG_BOUNDS == 0
     assert s1 == s0
@@ -71,6 +78,8 @@ def test_inference_under_bounds_checks(T, D, F, p, W, cap):
     for a, b in zip(_slots(h1), _slots(h0)):
         torch.testing.assert_close(a, b, rtol=0, atol=0)
     torch.testing.assert_close(h1.block_bits, h0.block_bits, rtol=0, atol=0)
+    # the one-kernel decode forward adds with atomics and drops no entry
+    torch.testing.assert_close(yd1, yd0, rtol=1e-5, atol=1e-6)
     if s0 != 0:
         # a full spill list: which slices got a slot depends on the order of
         # atomics, and the rows without one are undefined, so y is not compared

@@ -225,3 +225,84 @@ def test_decode_sweep(T):
     zg = _check_z(w, z)
     assert_twell_equal(fetch_twell(h), oracle.twell_pack(zg, 128, w.width))
     check_y(y.cpu().numpy().astype(np.float64), w, zg)
+
+
+# ------------------------------------------------- fused decode-sized forward
+
+DECODE_FUSED = [
+    # T, D, F, density, W
+    (1, 256, 1024, 0.05, 8),
+    (16, 2048, 1024, 0.01, 8),    # long rows: several 16-byte chunks per lane
+    (77, 72, 384, 0.10, 8),       # ragged T; D of two K blocks, not a multiple of 64
+    (129, 192, 640, 0.05, 1),     # W = 1; rank 1's tokens in both 128-token blocks
+    (200, 128, 1024, 0.50, 8),    # heavy spilling: every active entry still in y
+    (256, 512, 2048, 0.02, 16),   # the largest decode batch
+]
+
+
+@pytest.mark.parametrize("T,D,F,p,W", DECODE_FUSED)
+def test_ffn_decode_parity(T, D, F, p, W):
+    # one kernel: the TwELL bit-exact as twell_gate_pack packs it, y against
+    # the dense fp64 definition on the kernel's own fp32 gate decisions
+    w = workloads.random_small(T, D, F, p, W, seed=T + 3)
+    d = upload(w)
+    h = tw.TwELL(T, F, W)
+    z = torch.empty((T, F), dtype=torch.float32, device="cuda")
+    y = tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], h, z_debug=z)
+    torch.cuda.synchronize()
+    assert int(h.status.item()) == 0
+    zg = _check_z(w, z)
+    assert_twell_equal(fetch_twell(h), oracle.twell_pack(zg, 128, W))
+    np.testing.assert_array_equal(h.block_bits.cpu().numpy().view(np.uint32),
+                                  block_bits_reference(zg))
+    check_y(y.cpu().numpy().astype(np.float64), w, zg)
+    # the same TwELL through the separate fused kernel: equal to fp32 rounding
+    y2 = tw.twell_ffn_fwd(d["x"], h, d["Wu_t"], d["Wd"])
+    torch.cuda.synchronize()
+    scale = float(y2.abs().max()) + 1e-30
+    assert float((y - y2).abs().max()) <= 1e-5 * scale
+
+
+def test_ffn_decode_full_spill_list_drops_nothing():
+    # the spill list holds 4 slices: the TwELL flags it, but y still sums
+    # every positive gate value (the entries come from z, not from the list)
+    w = workloads.random_small(64, 128, 1024, 0.5, 8, seed=5)
+    d = upload(w)
+    h = tw.TwELL(w.T, w.F, 8, spill_cap=4)
+    z = torch.empty((w.T, w.F), dtype=torch.float32, device="cuda")
+    y = tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], h, z_debug=z)
+    torch.cuda.synchronize()
+    assert int(h.status.item()) == tw.FLAG_SPILL_FULL
+    zg = _check_z(w, z)
+    check_y(y.cpu().numpy().astype(np.float64), w, zg)
+
+
+def test_ffn_decode_limits():
+    w = workloads.random_small(257, 128, 256, 0.05, 8, seed=1)
+    d = upload(w)
+    with pytest.raises(tw.TwellError):
+        tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], tw.TwELL(257, 256, 8))
+    x0 = d["x"][:0]
+    y0 = tw.twell_ffn_decode(x0, d["Wg_t"], d["Wu_t"], d["Wd"], tw.TwELL(0, 256, 8))
+    assert y0.shape == (0, 128)
+    # repeated calls (y zeroed by each) agree to fp32 rounding
+    h = tw.TwELL(100, 256, 8)
+    x1 = d["x"][:100]
+    ya = tw.twell_ffn_decode(x1, d["Wg_t"], d["Wu_t"], d["Wd"], h).clone()
+    yb = tw.twell_ffn_decode(x1, d["Wg_t"], d["Wu_t"], d["Wd"], h)
+    torch.cuda.synchronize()
+    assert float((ya - yb).abs().max()) <= 1e-5 * (float(ya.abs().max()) + 1e-30)
+
+
+@pytest.mark.parametrize("T", workloads.DECODE_T)
+def test_ffn_decode_sweep(T):
+    w = workloads.config(4, T=T)
+    d = upload(w)
+    h = tw.TwELL(T, w.F, w.width)
+    z = torch.empty((T, w.F), dtype=torch.float32, device="cuda")
+    y = tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], h, z_debug=z)
+    torch.cuda.synchronize()
+    assert int(h.status.item()) == 0
+    zg = _check_z(w, z)
+    assert_twell_equal(fetch_twell(h), oracle.twell_pack(zg, 128, w.width))
+    check_y(y.cpu().numpy().astype(np.float64), w, zg)
