@@ -67,7 +67,7 @@ TRAFFIC = {
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
         775.73e6, "csrc/ffn_fwd.cu", "2ca95b29f788f850", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        149.71e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        149.95e6, "csrc/gate_pack.cu", "5e40b6905bb78535", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         212.57e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
@@ -76,7 +76,7 @@ TRAFFIC = {
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         105.91e6, "csrc/ffn_fwd.cu", "2ca95b29f788f850", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        45.02e6, "csrc/gate_pack.cu", "b1bd774522101e28", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        45.07e6, "csrc/gate_pack.cu", "5e40b6905bb78535", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
 
 

@@ -78,8 +78,9 @@ def test_inference_under_bounds_checks(T, D, F, p, W, cap):
     for a, b in zip(_slots(h1), _slots(h0)):
         torch.testing.assert_close(a, b, rtol=0, atol=0)
     torch.testing.assert_close(h1.block_bits, h0.block_bits, rtol=0, atol=0)
-    # the one-kernel decode forward adds with atomics and drops no entry
-    torch.testing.assert_close(yd1, yd0, rtol=1e-5, atol=1e-6)
+    # the one-kernel decode forward adds whole rows with atomics in any order
+    # (up to F terms per element): equal to fp32 rounding of the largest terms
+    torch.testing.assert_close(yd1, yd0, rtol=1e-5, atol=1e-5 * float(yd0.abs().max()))
     if s0 != 0:
         # a full spill list: which slices got a slot depends on the order of
         # atomics, and the rows without one are undefined, so y is not compared

@@ -237,6 +237,7 @@ DECODE_FUSED = [
     (129, 192, 640, 0.05, 1),     # W = 1; rank 1's tokens in both 128-token blocks
     (200, 128, 1024, 0.50, 8),    # heavy spilling: every active entry still in y
     (256, 512, 2048, 0.02, 16),   # the largest decode batch
+    (256, 2048, 256, 0.50, 8),    # half of all entries active: 8192 entries per CTA
 ]
 
 
