@@ -154,6 +154,31 @@ def test_gate_pack_wait_timeout_sets_flag_then_recovers(T, D, F):
     assert_twell_equal(fetch_twell(h2), oracle.twell_pack(zg, 128, 8))
 
 
+def test_ffn_decode_wait_timeout_sets_flag_then_recovers():
+    # the same 2 ns bound on the one-kernel decode step: its waits run out,
+    # it flags TWELL_FLAG_TIMEOUT, drains and skips the packing and the
+    # projection; the next call under the default bound is exact
+    w = workloads.random_small(64, 4096, 2048, 0.05, 8, seed=65)
+    d = upload(w)
+    h = tw.TwELL(w.T, w.F, 8)
+    torch.cuda.synchronize()
+    prev = tw.twell_gate_pack_wait_limit(2)
+    try:
+        tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], h)
+        torch.cuda.synchronize()
+    finally:
+        tw.twell_gate_pack_wait_limit(prev)
+    assert int(h.status.item()) & tw.FLAG_TIMEOUT
+    h2 = tw.TwELL(w.T, w.F, 8)
+    z = torch.empty((w.T, w.F), dtype=torch.float32, device="cuda")
+    y = tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], h2, z_debug=z)
+    torch.cuda.synchronize()
+    assert int(h2.status.item()) == 0
+    zg = _check_z(w, z)
+    assert_twell_equal(fetch_twell(h2), oracle.twell_pack(zg, 128, 8))
+    check_y(y.cpu().numpy().astype(np.float64), w, zg)
+
+
 def test_empty_batch_is_noop():
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     W = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
