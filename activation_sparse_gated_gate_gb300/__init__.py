@@ -231,10 +231,11 @@ def twell_gate_pack(x, Wg_t, out: TwELL, z_debug=None, status=None, stream=None)
 
 def twell_ffn_decode(x, Wg_t, Wu_t, Wd, out: TwELL, y=None, z_debug=None, status=None,
                      stream=None):
-    """Decode-sized forward in one kernel (1 <= T <= 256): the gate with its
+    """Decode-sized forward in one call (1 <= T <= 256): the gate with its
     TwELL epilogue into ``out`` (as ``twell_gate_pack``) and the up + down
-    projection of every active entry into y; returns y [T][D] fp32
-    (allocated if not given, zeroed by the call)."""
+    projection into y -- inside the gate kernel up to 8 tokens, else by the
+    CUDA-core fused kernel after a gate kernel that prefetched the active
+    rows; returns y [T][D] fp32 (allocated if not given, zeroed by the call)."""
     for t, name in ((x, "x"), (Wg_t, "Wg_t"), (Wu_t, "Wu_t"), (Wd, "Wd")):
         _need(t, torch.bfloat16, name)
     T, D = x.shape

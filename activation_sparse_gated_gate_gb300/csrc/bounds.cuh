@@ -36,4 +36,13 @@ __device__ __forceinline__ long long clamp_index(long long idx, long long n, int
   return in_bounds(idx, n, status) ? idx : 0;
 }
 
+// A TwELL column byte read as a column of its 128-wide tile: in the checking
+// build the byte as stored (its neuron's range is checked where it is used);
+// in the normal build its low seven bits, so a TwELL left undefined (by a
+// gate call whose wait ran out) can give wrong values downstream but never a
+// neuron outside its tile.
+__device__ __forceinline__ int tile_col(uint32_t byte) {
+  return static_cast<int>(kBoundsCheck ? byte : (byte & 127u));
+}
+
 }  // namespace twell

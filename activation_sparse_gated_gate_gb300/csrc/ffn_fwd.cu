@@ -206,14 +206,14 @@ __global__ void __launch_bounds__(warps_for(NC) * 32, 1) ffn_fwd_kernel(const Ff
                 for (int e = 0; e < 4; ++e) {
                   const int s = q + e;
                   if (s >= s0 && s < s1)
-                    list[off + s - base] = Entry{jbase + static_cast<int>((c4 >> (8 * e)) & 0xffu),
+                    list[off + s - base] = Entry{jbase + tile_col((c4 >> (8 * e)) & 0xffu),
                                                  vv[e], static_cast<int32_t>(so + s)};
                 }
               }
             } else {
               for (int s = s0; s < s1; ++s)
                 list[off + s - base] =
-                    Entry{jbase + p.col[so + s], p.val[so + s], static_cast<int32_t>(so + s)};
+                    Entry{jbase + tile_col(p.col[so + s]), p.val[so + s], static_cast<int32_t>(so + s)};
             }
           } else {
             const float* sl = p.spill_val + static_cast<size_t>(spill) * TWELL_TILE;

@@ -205,7 +205,7 @@ __device__ __forceinline__ void ug_walk_pair(const UgArgs& p, size_t rt, int k, 
     const uint8_t* cp = p.col + rt * p.W;
     const float* vp = p.val + rt * p.W;
     for (int s = 0; s < c; ++s) {
-      const int n = k * TWELL_TILE + cp[s];
+      const int n = k * TWELL_TILE + tile_col(cp[s]);
       if (in_bounds(n, p.F, p.status)) fn(n, vp[s]);
     }
   } else {
@@ -533,7 +533,7 @@ __device__ __forceinline__ void walk_tiles(const UgArgs& p, size_t rtb, int k0, 
       for (int e = 0; e < WV; ++e)
         if (e < cn[b]) {
           const int n =
-              (k + b) * TWELL_TILE + static_cast<int>((cw[b][e >> 2] >> (8 * (e & 3))) & 0xffu);
+              (k + b) * TWELL_TILE + tile_col((cw[b][e >> 2] >> (8 * (e & 3))) & 0xffu);
           if (in_bounds(n, p.F, p.status)) fn(n, vs[b][e]);
         }
     }

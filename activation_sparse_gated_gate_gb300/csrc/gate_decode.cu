@@ -314,6 +314,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_wait();  // the partner's partial sums and abort flag are here
 
   const bool go = !aborted_here && *peer_aborted == 0u;  // the same value in every thread
+  if (epi && !go) {
+    // nothing is packed: the tile's counts of this CTA's tokens say so, so
+    // a consumer of the TwELL (the CUDA-core kernel that twell_ffn_decode
+    // runs next, for one) finds it empty rather than undefined
+    const int t = own0 + (warp - 2) * 32 + lane;
+    if (t < own1 && t < p.T) p.cnt[static_cast<size_t>(t) * p.n_t + tile] = 0;
+  }
   if (epi && go) {
     ptx::tc_fence_after();
     const uint32_t lt = (1u << lane) - 1u;
@@ -378,34 +385,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           p.col[o] = static_cast<uint8_t>(n);
         }
       }
-      if (p.y) {
-        // every active entry of the chunk (slots and spill alike) into the
-        // CTA's list, and its neuron's W_u and W_d rows on their way to L2
-        int pre[16], tot = 0;
+      if (p.Wu_t) {
+        // the chunk's active neurons: their W_u and W_d rows on their way to
+        // L2, read next by the projection (in this kernel, or the CUDA-core
+        // forward right after it); with the projection here, every active
+        // entry (slots and spill alike) into the CTA's list
+        uint32_t mine = 0u;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          pre[j] = tot;
-          tot += __popc(m[j]);
-        }
-        if (tot > 0) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(n_ent, tot);
-          base = __shfl_sync(0xffffffffu, base, 0);
-          const size_t roff = (static_cast<size_t>(tile) * DM + n) * p.D;
-          bool mine = false;
+        for (int j = 0; j < 16; ++j) mine |= m[j];
+        if (p.y) {
+          int pre[16], tot = 0;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if ((m[j] >> lane) & 1u) {
-              const int idx = base + pre[j] + __popc(m[j] & lt);
-              if (in_bounds(idx, (own1 - own0) * DM, p.status))
-                ent[idx] = make_uint2(static_cast<uint32_t>((c + j) * DM + n), __float_as_uint(v[j]));
-              mine = true;
+            pre[j] = tot;
+            tot += __popc(m[j]);
+          }
+          if (tot > 0) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(n_ent, tot);
+            base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if ((m[j] >> lane) & 1u) {
+                const int idx = base + pre[j] + __popc(m[j] & lt);
+                if (in_bounds(idx, (own1 - own0) * DM, p.status))
+                  ent[idx] =
+                      make_uint2(static_cast<uint32_t>((c + j) * DM + n), __float_as_uint(v[j]));
+              }
             }
           }
-          if (mine) {
-            ptx::prefetch_l2_bulk(p.Wu_t + roff, static_cast<uint32_t>(p.D) * 2u);
-            ptx::prefetch_l2_bulk(p.Wd + roff, static_cast<uint32_t>(p.D) * 2u);
-          }
+        }
+        if ((mine >> lane) & 1u) {
+          const size_t roff = (static_cast<size_t>(tile) * DM + n) * p.D;
+          ptx::prefetch_l2_bulk(p.Wu_t + roff, static_cast<uint32_t>(p.D) * 2u);
+          ptx::prefetch_l2_bulk(p.Wd + roff, static_cast<uint32_t>(p.D) * 2u);
         }
       }
       if (spills != 0u) {
@@ -531,7 +544,7 @@ twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const 
   p.region = stages * p.stage_bytes;
   // the entry list of the fused projection: at most every neuron of every
   // token of rank 0 (the larger half)
-  if (ffn && p.region < p.half * DM * kEntryBytes) return TWELL_ERR_UNSUPPORTED;
+  if (ffn && ffn->y && p.region < p.half * DM * kEntryBytes) return TWELL_ERR_UNSUPPORTED;
   p.tmem_cols = 32;
   while (p.tmem_cols < static_cast<uint32_t>(p.N)) p.tmem_cols <<= 1;
   p.val = out->val;

@@ -43,6 +43,12 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+// twell_ffn_decode: the projection stays in the gate kernel up to this many
+// tokens (measured at d_model 2048, d_ff 8192, 0.5 %: the one-kernel step wins
+// at T = 1 and 4 and ties at 16), and for rows wider than the CUDA-core fused
+// kernel takes
+constexpr int32_t kDecodeProjectMaxT = 8;
+constexpr int32_t kFusedMaxD = 256 * 12;
 
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
@@ -442,7 +448,7 @@ extern "C" twell_status twell_ffn_decode(const uint16_t* x, const uint16_t* Wg_t
   twell_status st = check_twell(out, T, F, true);
   if (st != TWELL_OK) return st;
   if (T == 0) return TWELL_OK;
-  if (!x || !Wg_t || !Wu_t || !Wd || !y) return TWELL_ERR_INVALID;
+  if (!x || !Wg_t || !Wu_t || !Wd || !y || !status_dev) return TWELL_ERR_INVALID;
   if (!aligned16(x) || !aligned16(Wg_t) || !aligned16(Wu_t) || !aligned16(Wd) || !aligned16(y))
     return TWELL_ERR_INVALID;
   if (z_debug && !aligned16(z_debug)) return TWELL_ERR_INVALID;
@@ -451,11 +457,23 @@ extern "C" twell_status twell_ffn_decode(const uint16_t* x, const uint16_t* Wg_t
   if ((st = require_sm103(&dev)) != TWELL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out->spill_n, 0, sizeof(int32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
-  if (cudaMemsetAsync(y, 0, static_cast<size_t>(T) * D * sizeof(float), s) != cudaSuccess)
-    return TWELL_ERR_CUDA;
-  const DecodeFfn ffn{Wu_t, Wd, y};
-  return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev,
-                            g_wait_ns.load(std::memory_order_relaxed), &ffn, s);
+  const uint64_t wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  // A few tokens: the projection inside the gate kernel (each entry adds a
+  // whole row of y with atomics, cheap while entries are few).  More: the
+  // gate kernel prefetches the active rows into L2 and the CUDA-core fused
+  // kernel, which sums several entries per warp before its atomics, follows.
+  if (T <= kDecodeProjectMaxT || D > kFusedMaxD) {
+    if (cudaMemsetAsync(y, 0, static_cast<size_t>(T) * D * sizeof(float), s) != cudaSuccess)
+      return TWELL_ERR_CUDA;
+    const DecodeFfn ffn{Wu_t, Wd, y};
+    return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, wait_ns, &ffn,
+                              s);
+  }
+  const DecodeFfn prefetch{Wu_t, Wd, nullptr};
+  if ((st = launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, wait_ns,
+                               &prefetch, s)) != TWELL_OK)
+    return st;
+  return twell_ffn_fwd(x, out, Wu_t, Wd, D, y, status_dev, stream);
 }
 
 extern "C" uint64_t twell_gate_pack_wait_limit(uint64_t ns) {

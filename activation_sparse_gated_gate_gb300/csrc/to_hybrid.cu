@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
       const uint8_t* sc = p.col + (src_rt + k) * p.W;
       for (; s < c; ++s) {
         dv[s] = sv[s];
-        dc[s] = sc[s];
+        dc[s] = static_cast<uint8_t>(tile_col(sc[s]));
       }
     } else if (c > 0) {
       const float* sl = p.spill_val + static_cast<size_t>(slot) * TWELL_TILE;

@@ -132,15 +132,19 @@ twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T,
                              int32_t* status_dev, void* stream);
 
 /*
- * Decode-sized forward in one kernel (paper sections 2.B.1 and 2.B.2
+ * Decode-sized forward in one call (paper sections 2.B.1 and 2.B.2
  * together): the gate GEMM z = x W_g with its TwELL epilogue, exactly as
- * twell_gate_pack (same `out`, same z_debug), and in the same kernel, for
- * every active entry (t, j) of z -- slots and spill alike, so nothing is
- * dropped when the spill list is full -- u = x_t . W_u[:, j] (fp32) and
- * y_t += (h u) W_d[j, :] with fp32 atomics.  Rows with no active entry get
- * y_t = 0.
+ * twell_gate_pack (same `out`, same z_debug), then y = sum over the active
+ * entries (t, j) of (h u) W_d[j, :] with u = x_t . W_u[:, j] (fp32).  Up to 8
+ * tokens (or d_model > 3072) the projection runs inside the gate kernel: every
+ * active entry of z -- slots and spill alike, so nothing is dropped when the
+ * spill list is full -- adds its row to y with fp32 atomics.  With more
+ * tokens the gate kernel prefetches the active neurons' W_u and W_d rows
+ * into L2 while it packs, and the call then runs twell_ffn_fwd on the TwELL
+ * it wrote (whose rules then hold: a missing spill slice is skipped and
+ * flagged).  Rows with no active entry get y_t = 0.
  *   x   [T][D] bf16   Wg_t, Wu_t, Wd  [F][D] bf16   y  [T][D] fp32 (written;
- *   zeroed by the call, stream-ordered)
+ *   zeroed by the call, stream-ordered)   status_dev  device int32 (required)
  * Supports 1 <= T <= 256 with D > 64 (TWELL_ERR_UNSUPPORTED otherwise:
  * use twell_gate_pack + twell_ffn_fwd); D % 8 == 0, all pointers 16-byte
  * aligned.  Repeats agree to fp32 rounding, not bit for bit (atomics).
