@@ -27,9 +27,9 @@
 // tokens with similar counts of active neurons have a smaller total union
 // than blocks of consecutive tokens wherever the per-token activity varies
 // (a heavy-tailed batch: 55 % of d_ff per block instead of 73 % in the
-// 1.5B-class workload).  Three small kernels sort the tokens, stably, by a
+// 1.5B-class workload).  Two small kernels sort the tokens, stably, by a
 // logarithmic bucket of their active count (eight buckets per octave) into a
-// permutation; a fourth copies x into that order for the up GEMM's TMA
+// permutation; a third copies x into that order for the up GEMM's TMA
 // tiles, the down epilogue writes each y row to its token, and the rest of
 // the pipeline works on token positions.  In a batch whose tokens are about
 // equally active the sort gains nothing and costs its kernels, so the plain
@@ -182,9 +182,8 @@ UgLayout ug_layout(int64_t T, int64_t D, int64_t F, bool sorted) {
 }
 
 // ------------------------------------------------------------ preparation
-//   ug_key_kernel, ug_hist_scan_kernel, ug_place_kernel  sort the tokens
-//                   into positions (see the header); ug_perm_x_kernel copies
-//                   x into position order.
+//   ug_key_kernel, ug_place_kernel  sort the tokens into positions (see the
+//                   header); ug_perm_x_kernel copies x into position order.
 //   ug_bits_kernel  (grid: blocks x 8 CTAs of 16 positions) ORs every active
 //                   neuron of its positions' tokens into the block's union
 //                   bitmap (shared memory, then global atomics into the
@@ -259,34 +258,46 @@ __global__ void __launch_bounds__(UG_SORT_THREADS) ug_key_kernel(const UgArgs p)
     p.hist[static_cast<size_t>(blockIdx.x) * UG_NBUCKET + i] = h[i];
 }
 
-// One CTA: hist[c][b] becomes the first position of bucket b's tokens of
-// sort CTA c (buckets in order, CTAs in order within a bucket).
-__global__ void __launch_bounds__(UG_NBUCKET) ug_hist_scan_kernel(const UgArgs p) {
-  __shared__ int tot[UG_NBUCKET];
-  const int b = threadIdx.x;
-  int sum = 0;
-  for (int c = 0; c < p.n_sort; ++c) sum += p.hist[static_cast<size_t>(c) * UG_NBUCKET + b];
-  tot[b] = sum;
-  __syncthreads();
-  int start = 0;
-  for (int i = 0; i < b; ++i) start += tot[i];
-  for (int c = 0; c < p.n_sort; ++c) {
-    int* hp = p.hist + static_cast<size_t>(c) * UG_NBUCKET + b;
-    const int v = *hp;
-    *hp = start;
-    start += v;
-  }
-}
-
 // One thread per token: its position = the start of its bucket in its sort
-// CTA + the tokens of the same bucket before it in the CTA (warp match and
-// per-warp counts), so the order is stable.
+// CTA (the tokens of lower buckets, then those of its bucket in earlier sort
+// CTAs, both from the per-CTA histograms) + the tokens of the same bucket
+// before it in the CTA (warp match and per-warp counts), so the order is
+// stable.
 __global__ void __launch_bounds__(UG_SORT_THREADS) ug_place_kernel(const UgArgs p) {
   constexpr int kWarps = UG_SORT_THREADS / 32;
   __shared__ int wc[kWarps][UG_NBUCKET];
+  __shared__ int start[UG_NBUCKET];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kWarps * UG_NBUCKET; i += UG_SORT_THREADS)
     wc[i / UG_NBUCKET][i % UG_NBUCKET] = 0;
+  if (warp < UG_NBUCKET / 32) {
+    // bucket b = 32 warp + lane: its total over all sort CTAs and its count
+    // in the CTAs before this one, then the exclusive prefix of the totals
+    const int b = warp * 32 + lane;
+    int total = 0, before = 0;
+    for (int c = 0; c < p.n_sort; ++c) {
+      const int v = p.hist[static_cast<size_t>(c) * UG_NBUCKET + b];
+      total += v;
+      if (c < static_cast<int>(blockIdx.x)) before += v;
+    }
+    int incl = total;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    wc[0][b] = incl;  // the warps' inclusive sums, combined below
+    start[b] = before - total;
+  }
+  __syncthreads();
+  if (warp < UG_NBUCKET / 32) {
+    const int b = warp * 32 + lane;
+    int lower = 0;  // totals of the earlier warps' buckets
+    for (int w = 0; w < warp; ++w) lower += wc[0][w * 32 + 31];
+    start[b] += wc[0][b] + lower;  // = exclusive prefix of totals + before
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < UG_NBUCKET; i += UG_SORT_THREADS) wc[0][i] = 0;
   __syncthreads();
   const int t = blockIdx.x * UG_SORT_THREADS + threadIdx.x;
   const bool valid = t < p.T;
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(UG_SORT_THREADS) ug_place_kernel(const UgArgs 
   }
   __syncthreads();
   if (valid) {
-    const int pos = p.hist[static_cast<size_t>(blockIdx.x) * UG_NBUCKET + b] + wc[warp][b] + rank;
+    const int pos = start[b] + wc[warp][b] + rank;
     if (in_bounds(pos, p.T, p.status)) p.perm[pos] = t;
   }
 }
@@ -1082,7 +1093,6 @@ twell_status ffn_tc_run(const uint16_t* x, const twell_t* h, const uint16_t* Wu_
   if (sorted) {
     // token order, then x in that order
     ug_key_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
-    ug_hist_scan_kernel<<<1, UG_NBUCKET, 0, s>>>(a);
     ug_place_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
     const long long n16 = static_cast<long long>(T) * (D / 8);
     const long long want = (n16 + 255) / 256;

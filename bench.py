@@ -61,22 +61,22 @@ METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of ro
 TRAFFIC = {
     # 1.5B-class layer (profiles/ffn_fwd_tc_1.5B_T16384.md)
     ("twell_ffn_fwd_tc_sorted", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        728.36e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        724.83e6, "csrc/ffn_tc.cu", "643203228694cf48", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        789.81e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        787.31e6, "csrc/ffn_tc.cu", "643203228694cf48", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        775.73e6, "csrc/ffn_fwd.cu", "2ca95b29f788f850", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        775.28e6, "csrc/ffn_fwd.cu", "69ac3bf21e44a5d5", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        149.95e6, "csrc/gate_pack.cu", "5e40b6905bb78535", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        149.52e6, "csrc/gate_pack.cu", "d2486faee81ad268", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        212.57e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        211.86e6, "csrc/ffn_tc.cu", "643203228694cf48", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc_sorted", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        238.87e6, "csrc/ffn_tc.cu", "9c809d2616e1dd7f", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        238.33e6, "csrc/ffn_tc.cu", "643203228694cf48", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        105.91e6, "csrc/ffn_fwd.cu", "2ca95b29f788f850", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        105.81e6, "csrc/ffn_fwd.cu", "69ac3bf21e44a5d5", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        45.07e6, "csrc/gate_pack.cu", "5e40b6905bb78535", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        45.03e6, "csrc/gate_pack.cu", "d2486faee81ad268", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
 
 
@@ -688,19 +688,23 @@ class InferCase:
 FWD_NAMES = {"tc": "twell_ffn_fwd_tc", "tcs": "twell_ffn_fwd_tc_sorted", "cc": "twell_ffn_fwd",
              "dec": "twell_ffn_decode"}
 # kernels of the library launched by one forward call: union scan + up +
-# down GEMMs; the sorted variant adds three sort kernels, the x copy and the
+# down GEMMs; the sorted variant adds two sort kernels, the x copy and the
 # union bitmaps; the CUDA-core forward is one kernel (the gate is one more);
 # the one-kernel decode forward includes the gate
-FWD_LAUNCHES = {"tc": 3, "tcs": 8, "cc": 1, "dec": 1}
+FWD_LAUNCHES = {"tc": 3, "tcs": 7, "cc": 1, "dec": 2}
 
 
-def iter_launches(kinds):
+def iter_launches(kinds, T=None):
     """Library kernels per timed iteration of infer_entry: the gate graph,
     each forward's graph and each step's graph (gate + forward; the decode
-    forward's step is its one kernel)."""
+    call's step is its gate kernel, followed above 8 tokens by the CUDA-core
+    kernel)."""
     n = 1
     for kd in kinds:
-        n += FWD_LAUNCHES[kd] if kd == "dec" else 1 + 2 * FWD_LAUNCHES[kd]
+        if kd == "dec":
+            n += 1 if T is not None and T <= 8 else FWD_LAUNCHES["dec"]
+        else:
+            n += 1 + 2 * FWD_LAUNCHES[kd]
     return n
 
 
@@ -807,7 +811,7 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
         "timing": ("each call and each step captured as a CUDA graph, replayed after an L2 "
                    "flush between CUDA events; mean of K"),
     }
-    entry["launches_per_iteration"] = iter_launches(kinds)
+    entry["launches_per_iteration"] = iter_launches(kinds, w.T)
     fwd_ms = t["step_dec"] if best == "dec" else t[best]
     return entry, {"use": best, "fwd_ms": fwd_ms, "gate_ms": 0.0 if best == "dec" else g_ms,
                    "fwd_name": FWD_NAMES[best], "nnz": nnz, "n_active": n_active,
