@@ -29,8 +29,8 @@
 // (a heavy-tailed batch: 55 % of d_ff per block instead of 73 % in the
 // 1.5B-class workload).  Two small kernels sort the tokens, stably, by a
 // logarithmic bucket of their active count (eight buckets per octave) into a
-// permutation; a third copies x into that order for the up GEMM's TMA
-// tiles, the down epilogue writes each y row to its token, and the rest of
+// permutation; the union-bitmap kernel also copies x into that order for the
+// up GEMM's TMA tiles, the down epilogue writes each y row to its token, and the rest of
 // the pipeline works on token positions.  In a batch whose tokens are about
 // equally active the sort gains nothing and costs its kernels, so the plain
 // entry point keeps blocks of consecutive tokens.
@@ -183,11 +183,12 @@ UgLayout ug_layout(int64_t T, int64_t D, int64_t F, bool sorted) {
 
 // ------------------------------------------------------------ preparation
 //   ug_key_kernel, ug_place_kernel  sort the tokens into positions (see the
-//                   header); ug_perm_x_kernel copies x into position order.
+//                   header).
 //   ug_bits_kernel  (grid: blocks x 8 CTAs of 16 positions) ORs every active
 //                   neuron of its positions' tokens into the block's union
 //                   bitmap (shared memory, then global atomics into the
-//                   zeroed [n_m][nw] bitmap).
+//                   zeroed [n_m][nw] bitmap); in sorted order it also copies
+//                   its positions' x rows into position order.
 //   ug_scan_kernel  (one CTA per block) takes the exclusive prefix of the
 //                   bitmap words' popcounts -- a neuron's union position is
 //                   the prefix of its word plus the set bits below it in the
@@ -322,20 +323,6 @@ __global__ void __launch_bounds__(UG_SORT_THREADS) ug_place_kernel(const UgArgs 
   }
 }
 
-// xp[i] = x[perm[i]] (rows of D bf16, 16 bytes per step).
-__global__ void __launch_bounds__(256) ug_perm_x_kernel(const UgArgs p) {
-  const int per_row = p.D / 8;
-  const long long total = static_cast<long long>(p.T) * per_row;
-  for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
-       v += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(v / per_row);
-    const int q = static_cast<int>(v % per_row);
-    const int t = static_cast<int>(clamp_index(p.perm[i], p.T, p.status));
-    reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(i) * p.D)[q] =
-        __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.D) + q);
-  }
-}
-
 __global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p) {
   extern __shared__ uint32_t psm[];
   const int nw = p.nw;
@@ -345,6 +332,19 @@ __global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p
   const int rows = min(UG_ROWS_PER_CTA, p.T - r0);
   if (rows <= 0) return;
   for (int i = threadIdx.x; i < nw; i += UG_PREP_THREADS) bm[i] = 0u;
+  if (p.xp) {
+    // sorted order: the CTA's positions' x rows, xp[i] = x[perm[i]], for the
+    // up GEMM's TMA tiles (16-byte steps; bandwidth-bound, it overlaps the
+    // latency-bound walk below across the CTAs of an SM)
+    const int per_row = p.D / 8;
+    for (int i = threadIdx.x; i < rows * per_row; i += UG_PREP_THREADS) {
+      const int r = i / per_row;
+      const int q = i - r * per_row;
+      const int t = static_cast<int>(clamp_index(p.perm[r0 + r], p.T, p.status));
+      reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(r0 + r) * p.D)[q] =
+          __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.D) + q);
+    }
+  }
   __syncthreads();
   const int n_t = p.n_t;
   for (int q = threadIdx.x; q < rows * n_t; q += UG_PREP_THREADS) {
@@ -1094,10 +1094,6 @@ twell_status ffn_tc_run(const uint16_t* x, const twell_t* h, const uint16_t* Wu_
     // token order, then x in that order
     ug_key_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
     ug_place_kernel<<<a.n_sort, UG_SORT_THREADS, 0, s>>>(a);
-    const long long n16 = static_cast<long long>(T) * (D / 8);
-    const long long want = (n16 + 255) / 256;
-    const long long cap = 8ll * dev.sm_count;
-    ug_perm_x_kernel<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(a);
   }
   const dim3 pgrid(a.n_m, UG_BM / UG_ROWS_PER_CTA);
   if (own_bits) {
