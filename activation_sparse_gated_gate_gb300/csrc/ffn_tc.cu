@@ -35,6 +35,10 @@
 // equally active the sort gains nothing and costs its kernels, so the plain
 // entry point keeps blocks of consecutive tokens.
 //
+// A block whose union is nearly every neuron runs dense: U is then every
+// neuron in order, its weight tiles are contiguous and come by TMA (about
+// 1.26 times the tensor-pipe rate of the row gathers).
+//
 // The union bitmap of each block comes from the gate kernel (TwELL
 // block_bits, blocks of consecutive tokens only) or from a small kernel over
 // the TwELL entries of its tokens; a scan kernel turns it into U (padded
@@ -80,6 +84,15 @@ constexpr int UG_EPI = 256;             // epilogue threads: two sets of four wa
 constexpr int UG_GATHER0 = 64 + UG_EPI; // first thread of the gather groups
 constexpr int UG_THREADS = UG_GATHER0 + UG_ST * UG_GROUP;
 constexpr int UG_HSLOTS = 16;           // up epilogue: gate values staged per row and set
+// A block whose union holds at least this percentage of the neurons runs as
+// a dense block (every neuron, weight tiles by TMA instead of row gathers).
+// Measured at the 1.5B-class layer: a dense block costs about 1 / 1.26 of a
+// gathered block of the same width, so the whole tile wins from a union of
+// about 80 % (thresholds 60 / 70 / 80 % / never: sorted call 529 / 514 / 513 /
+// 531 us, and 70 % made the plain call's 72 % unions slower, 632 against 571).
+#ifndef UG_DENSE_PCT
+#define UG_DENSE_PCT 80
+#endif
 
 // Shared memory: [stages][output staging: 8 epilogue warps x one 32 x 32
 // chunk][barriers 256 B][up: gate-value slots 2 sets x 128 rows x UG_HSLOTS fp32]
@@ -114,7 +127,9 @@ struct UgArgs {
   int32_t* ctr;     // [0]: units of the up GEMM
   uint32_t* gbm;    // [n_m][gbm_pitch] union bitmap of each block (F / 32 words used)
   int32_t gbm_pitch;
-  int32_t* nU;      // [n_m] union sizes
+  int32_t* nU;      // [n_m] union sizes (a dense block: F)
+  int8_t* dense;    // [n_m] 1: the block's union is every neuron (see UG_DENSE_PCT)
+  int32_t dense_min;  // union size from which a block runs dense (0: never)
   int32_t* Ulist;   // [n_m][Fp] union neurons, ascending, padded with 0
   int32_t* units;   // [n_m * nj] up-GEMM units (block * nj + chunk)
   int32_t* wpre;    // [n_m][nw] union position of each bitmap word's first bit
@@ -134,7 +149,7 @@ constexpr int UG_SORT_THREADS = 1024;  // tokens per sort CTA
 constexpr int UG_NBUCKET = 128;        // activity buckets (eight per octave)
 
 struct UgLayout {
-  size_t ctr, gbm, nU, Ulist, units, wpre, abuf, wd16, perm, keys, hist, xp, bytes;
+  size_t ctr, gbm, nU, dense, Ulist, units, wpre, abuf, wd16, perm, keys, hist, xp, bytes;
   int64_t Fp, nw, n_m, nj, n_sort;
 };
 
@@ -153,6 +168,8 @@ UgLayout ug_layout(int64_t T, int64_t D, int64_t F, bool sorted) {
   o = up256(o + static_cast<size_t>(L.n_m) * L.nw * 4);
   L.nU = o;
   o = up256(o + L.n_m * 4);
+  L.dense = o;
+  o = up256(o + L.n_m);
   L.Ulist = o;
   o = up256(o + static_cast<size_t>(L.n_m) * L.Fp * 4);
   L.units = o;
@@ -410,24 +427,32 @@ __global__ void __launch_bounds__(UG_PREP_THREADS) ug_scan_kernel(const UgArgs p
     }
     ex += c[e];
   }
-  const int nU = s_total;
+  // a union this large runs as a dense block: every neuron, in order, so
+  // its weight rows are contiguous and come by TMA instead of row gathers
+  const bool dense = p.dense_min > 0 && s_total >= p.dense_min;
+  const int nU = dense ? p.F : s_total;
   const int chunks = (nU + 255) >> 8;
   if (tid == 0) {
     p.nU[m] = nU;
+    p.dense[m] = dense ? 1 : 0;
     s_base = chunks > 0 ? atomicAdd(p.ctr, chunks) : 0;
   }
   __syncthreads();
   int32_t* Ul = p.Ulist + static_cast<size_t>(m) * p.Fp;
-  for (int w = tid; w < nw; w += UG_PREP_THREADS) {
-    uint32_t bits = bm[w];
-    int r = wpre[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      Ul[r++] = 32 * w + b;
+  if (dense) {
+    for (int i = tid; i < chunks * 256; i += UG_PREP_THREADS) Ul[i] = i < p.F ? i : 0;
+  } else {
+    for (int w = tid; w < nw; w += UG_PREP_THREADS) {
+      uint32_t bits = bm[w];
+      int r = wpre[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        Ul[r++] = 32 * w + b;
+      }
     }
+    for (int i = nU + tid; i < chunks * 256; i += UG_PREP_THREADS) Ul[i] = 0;
   }
-  for (int i = nU + tid; i < chunks * 256; i += UG_PREP_THREADS) Ul[i] = 0;
   for (int jn = tid; jn < chunks; jn += UG_PREP_THREADS) p.units[s_base + jn] = m * p.nj + jn;
 }
 
@@ -570,7 +595,8 @@ __device__ __forceinline__ float twell_h_at(const UgArgs& p, int t, int n) {
 template <int MODE>
 __global__ void __launch_bounds__(UG_THREADS, 1)
     ug_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_out, const UgArgs p) {
+                   const __grid_constant__ CUtensorMap map_out,
+                   const __grid_constant__ CUtensorMap map_b, const UgArgs p) {
   using SM = UgSmem<MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -721,6 +747,32 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       const int seq0 = seq;
       seq += U.kb;
       if (kb >= U.kb) continue;
+      if (p.dense[U.m]) {
+        // a dense block's tile: its B rows are contiguous (union position =
+        // neuron), one TMA box per stage (up: 256 neurons x 64 K of W_u^T;
+        // down: four 64 x 64 boxes of W_d16) issued by the group's first
+        // thread; the group still makes its 64 arrivals
+        for (; kb < U.kb; kb += UG_ST) {
+          const uint32_t phase = static_cast<uint32_t>((seq0 + kb) / UG_ST) & 1u;
+          if (!ptx::mbar_wait(eb, phase ^ 1u)) {
+            { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+            goto done;
+          }
+          if (g == 0) {
+            ptx::mbar_arrive_expect_tx(fb, UG_B);
+            if (MODE == UG_UP) {
+              ptx::tma_load_2d(sBp, &map_b, fb, kb * UG_BK, U.n0);
+            } else {
+#pragma unroll
+              for (int b4 = 0; b4 < 4; ++b4)
+                ptx::tma_load_2d(sBp + b4 * 8192, &map_b, fb, U.n0 + 64 * b4, kb * UG_BK);
+            }
+          } else {
+            ptx::mbar_arrive(fb);
+          }
+        }
+        continue;
+      }
       int col = 0;
       uint32_t nbytes = 16;
       if (MODE == UG_UP) {
@@ -823,12 +875,14 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           const int hi_n = __ldg(Ul + min(ps + 127, nUm - 1));
           const uint32_t* bmr = p.gbm + static_cast<size_t>(U.m) * p.gbm_pitch;
           const int32_t* wpr = p.wpre + static_cast<size_t>(U.m) * p.nw;
+          const bool dense_blk = p.dense[U.m] != 0;
           int nset = 0;
           auto add = [&](int n, float h) {
             if (n < lo_n || n > hi_n) return;
             const int w = n >> 5;
-            const int pos =
-                __ldg(wpr + w) + __popc(__ldg(bmr + w) & ((1u << (n & 31)) - 1u)) - ps;
+            const int pos = dense_blk ? n - ps
+                                    : __ldg(wpr + w) +
+                                          __popc(__ldg(bmr + w) & ((1u << (n & 31)) - 1u)) - ps;
             const uint32_t bit = 1u << (pos & 31);
             const uint32_t wsel = pos >> 5;  // a select per word, not an index
 #pragma unroll
@@ -970,8 +1024,9 @@ done:
 }
 
 template <int MODE>
-twell_status ug_launch(const CUtensorMap& map, const CUtensorMap& map_out, const UgArgs& a,
-                       int max_units, const DeviceInfo& dev, cudaStream_t s) {
+twell_status ug_launch(const CUtensorMap& map, const CUtensorMap& map_out,
+                       const CUtensorMap& map_b, const UgArgs& a, int max_units,
+                       const DeviceInfo& dev, cudaStream_t s) {
   constexpr int SMEM = UgSmem<MODE>::BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
   auto kern = ug_gemm_kernel<MODE>;
@@ -980,7 +1035,7 @@ twell_status ug_launch(const CUtensorMap& map, const CUtensorMap& map_out, const
     return TWELL_ERR_CUDA;
   if (max_units <= 0) return TWELL_OK;
   const int grid = max_units < dev.sm_count ? max_units : dev.sm_count;
-  kern<<<grid, UG_THREADS, SMEM, s>>>(map, map_out, a);
+  kern<<<grid, UG_THREADS, SMEM, s>>>(map, map_out, map_b, a);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
@@ -1062,6 +1117,8 @@ twell_status ffn_tc_run(const uint16_t* x, const twell_t* h, const uint16_t* Wu_
   a.gbm = own_bits ? reinterpret_cast<uint32_t*>(w + L.gbm) : h->block_bits;
   a.gbm_pitch = own_bits ? static_cast<int32_t>(L.nw) : F / 32;
   a.nU = reinterpret_cast<int32_t*>(w + L.nU);
+  a.dense = reinterpret_cast<int8_t*>(w + L.dense);
+  a.dense_min = static_cast<int32_t>((static_cast<int64_t>(F) * UG_DENSE_PCT + 99) / 100);
   a.Ulist = reinterpret_cast<int32_t*>(w + L.Ulist);
   a.units = reinterpret_cast<int32_t*>(w + L.units);
   a.wpre = reinterpret_cast<int32_t*>(w + L.wpre);
@@ -1078,13 +1135,21 @@ twell_status ffn_tc_run(const uint16_t* x, const twell_t* h, const uint16_t* Wu_
 
   // operand maps (box 64 x 128, 128-byte swizzle) and output maps (box
   // 32 x 32: a in bf16 with the 64-byte swizzle, y in fp32 with 128)
-  CUtensorMap map_x, map_a, map_as, map_y;
+  CUtensorMap map_x, map_a, map_as, map_y, map_wu, map_wd;
   if ((st = tc_map_a(&map_x, sorted ? a.xp : x, T, D, 0)) != TWELL_OK) return st;
   if ((st = tc_map_a(&map_a, a.abuf, T, L.Fp, 0)) != TWELL_OK) return st;
   if ((st = make_tmap_2d(&map_as, 2, a.abuf, L.Fp, T, 32, 32, L.Fp * 2, 64)) != TWELL_OK)
     return st;
   if ((st = make_tmap_2d(&map_y, 4, y, D, T, 32, 32, static_cast<uint64_t>(D) * 4, 128)) !=
       TWELL_OK)
+    return st;
+  // dense blocks' weight tiles: W_u^T 256 neurons x 64 K (K-major), W_d16
+  // 64 neurons x 64 outputs (N-major), both with the 128-byte swizzle
+  if ((st = make_tmap_2d(&map_wu, 2, Wu_t, D, F, UG_BK, UG_BN, static_cast<uint64_t>(D) * 2,
+                         128)) != TWELL_OK)
+    return st;
+  if ((st = make_tmap_2d(&map_wd, 2, a.Wd16, D, F, 64, UG_BK, static_cast<uint64_t>(D) * 2,
+                         128)) != TWELL_OK)
     return st;
 
   // the counter and our block bitmaps are adjacent: one memset clears both
@@ -1110,8 +1175,9 @@ twell_status ffn_tc_run(const uint16_t* x, const twell_t* h, const uint16_t* Wu_
                                                                            status_dev);
     if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
   }
-  if ((st = ug_launch<UG_UP>(map_x, map_as, a, a.n_m * a.nj, dev, s)) != TWELL_OK) return st;
-  return ug_launch<UG_DOWN>(map_a, map_y, a, a.n_m * a.nN, dev, s);
+  if ((st = ug_launch<UG_UP>(map_x, map_as, map_wu, a, a.n_m * a.nj, dev, s)) != TWELL_OK)
+    return st;
+  return ug_launch<UG_DOWN>(map_a, map_y, map_wd, a, a.n_m * a.nN, dev, s);
 }
 
 }  // namespace
