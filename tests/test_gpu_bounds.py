@@ -12,7 +12,6 @@ result equals the normal build's (bit for bit where the kernels are
 deterministic, to fp32 rounding where they add with atomics).  One TwELL
 whose column names a neuron past d_ff is then fed to the checking build only:
 the flag is set and the access is redirected, never made."""
-import numpy as np
 import pytest
 import torch
 

@@ -1,7 +1,6 @@
 """Pins of the oracle's bf16 rounding against torch's CPU conversion (a
 library routine) and hand-checked values."""
 import numpy as np
-import pytest
 import torch
 
 import oracle

@@ -7,7 +7,6 @@ caller workspace) on two calls in a row: the shared array keeps the first
 call's contents, and the second call must not depend on them.  This file is
 collected last so a run stopping at its first failure has run every other
 test."""
-import numpy as np
 import pytest
 import torch
 
