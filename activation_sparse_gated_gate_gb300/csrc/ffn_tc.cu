@@ -48,8 +48,16 @@
 // chunk's MMAs run.
 //
 // Both GEMMs: one persistent CTA per SM, tiles of 128 x 256 outputs, K in
-// blocks of 64, four shared-memory stages [A 16 KB][B 32 KB]:
-//   warp 0      TMA producer of the A tiles
+// blocks of 64, four shared-memory stages [A 16 KB][B 32 KB].  A CTA takes
+// its units (tiles) one at a time from a ticket counter of the launch, not a
+// fixed share: unit costs differ (dense or gathered weight tiles, union
+// sizes, heavy rows in the up epilogue), and a fixed round-robin share left
+// the average SM idle for a quarter of the sorted call's up GEMM at the
+// 1.5B-class layer (max / mean active cycles 1.28; with tickets 1.12, the
+// call 526 -> 497 us).  The producer claims the next unit near the end of
+// the current one and hands its record to the other roles through a ring of
+// unit records in shared memory.  Roles:
+//   warp 0      TMA producer of the A tiles, unit tickets
 //   warp 1      TMEM allocation (two 256-column accumulators) and MMA issue
 //   warps 2-9   epilogue: two sets of four warps, one TMEM lane quarter per
 //               warp; set s writes columns 128 s .. 128 s + 127 of the tile
@@ -84,6 +92,9 @@ constexpr int UG_EPI = 256;             // epilogue threads: two sets of four wa
 constexpr int UG_GATHER0 = 64 + UG_EPI; // first thread of the gather groups
 constexpr int UG_THREADS = UG_GATHER0 + UG_ST * UG_GROUP;
 constexpr int UG_HSLOTS = 16;           // up epilogue: gate values staged per row and set
+constexpr int UG_RING = 8;              // unit records in flight between the roles
+// arrivals that free a unit-ring slot: the MMA thread, each gather warp, each epilogue warp
+constexpr int UG_RING_READERS = 1 + UG_ST * UG_GROUP / 32 + UG_EPI / 32;
 // A block whose union holds at least this percentage of the neurons runs as
 // a dense block (every neuron, weight tiles by TMA instead of row gathers).
 // Measured at the 1.5B-class layer: a dense block costs about 1 / 1.26 of a
@@ -95,13 +106,14 @@ constexpr int UG_HSLOTS = 16;           // up epilogue: gate values staged per r
 #endif
 
 // Shared memory: [stages][output staging: 8 epilogue warps x one 32 x 32
-// chunk][barriers 256 B][up: gate-value slots 2 sets x 128 rows x UG_HSLOTS fp32]
+// chunk][barriers and the unit ring 512 B][up: gate-value slots 2 sets x 128
+// rows x UG_HSLOTS fp32]
 template <int MODE>
 struct UgSmem {
   static constexpr int STG_BUF = MODE == 0 ? 32 * 32 * 2 : 32 * 32 * 4;
   static constexpr int STG = UG_ST * UG_STAGE;
   static constexpr int BARS = STG + 8 * STG_BUF;
-  static constexpr int SLOTS = BARS + 256;
+  static constexpr int SLOTS = BARS + 512;
   static constexpr int BYTES = SLOTS + (MODE == 0 ? 2 * UG_BM * UG_HSLOTS * 4 : 0) + 1024;
 };
 constexpr int UG_PREP_THREADS = 256;
@@ -124,7 +136,8 @@ struct UgArgs {
   uint16_t* Wd16;       // fp16 copy in the workspace (the down GEMM's B)
   float* y;
   // workspace
-  int32_t* ctr;     // [0]: units of the up GEMM
+  int32_t* ctr;     // [0]: units of the up GEMM; [1], [2]: next-unit tickets of the up and
+                    // down GEMMs (zero before the launch)
   uint32_t* gbm;    // [n_m][gbm_pitch] union bitmap of each block (F / 32 words used)
   int32_t gbm_pitch;
   int32_t* nU;      // [n_m] union sizes (a dense block: F)
@@ -608,14 +621,15 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // abort path: MMA drain
   volatile uint32_t* aborted = tmem_slot + 1;
+  // unit ring: the producer publishes each unit's record, every other role
+  // reads it (barrier area bytes 128 .. 383)
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + SM::BARS + 128);
+  uint64_t* rempty = rfull + UG_RING;
+  UgUnit* ring = reinterpret_cast<UgUnit*>(smem + SM::BARS + 256);
   float* hslots = reinterpret_cast<float*>(smem + SM::SLOTS);  // up: [2][128][UG_HSLOTS]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_units = MODE == UG_UP ? *p.ctr : p.n_m * p.nN;
-  // every role reads the next unit's record one unit ahead
-  UgUnit Un{};
-  if (static_cast<int>(blockIdx.x) < num_units) Un = ug_unit<MODE>(p, blockIdx.x);
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < UG_ST; ++s) {
@@ -625,6 +639,10 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], UG_EPI);
+    }
+    for (int r = 0; r < UG_RING; ++r) {
+      ptx::mbar_init(&rfull[r], 1);
+      ptx::mbar_init(&rempty[r], UG_RING_READERS);
     }
     ptx::mbar_init(drain, 1);
     *aborted = 0u;
@@ -641,13 +659,56 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------- TMA producer (A)
+    // It also hands out the work: units go to CTAs in the order they ask,
+    // from a ticket counter of the launch (the costs of units differ: dense
+    // or gathered weight tiles, union sizes, rows with many entries in the
+    // up epilogue), and each unit's record goes to the other roles through
+    // the unit ring.  The down GEMM takes its units last to first: blocks of
+    // activity-sorted tokens come in ascending activity, so the largest
+    // unions go first.  A unit index past the count ends every role's loop.
     if (lane == 0) {
+      const int num_units = MODE == UG_UP ? *p.ctr : p.n_m * p.nN;
+      int* ticket = p.ctr + 1 + MODE;
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      int rs = 0;
+      uint32_t rph = 0;
+      auto unit_of = [&](int tk) {
+        return tk < num_units ? ug_unit<MODE>(p, MODE == UG_DOWN ? num_units - 1 - tk : tk)
+                              : UgUnit{-1, 0, 0, 0};
+      };
+      // a unit's record into the next ring slot (false: the wait ran out)
+      auto publish = [&](const UgUnit& V) {
+        if (!ptx::mbar_wait(&rempty[rs], rph ^ 1u)) return false;
+        ring[rs] = V;
+        ptx::mbar_arrive(&rfull[rs]);
+        if (++rs == UG_RING) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        return true;
+      };
+      UgUnit Un = unit_of(atomicAdd(ticket, 1));
+      bool published = false;  // Un is in the ring already
+      for (;;) {
         const UgUnit U = Un;
-        if (u + static_cast<int>(gridDim.x) < num_units)
-          Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
+        if (!published && !publish(U)) {
+          { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+          goto done;
+        }
+        published = false;
+        if (U.m < 0) break;
+        // The next unit is claimed ten tiles before this unit's last is
+        // issued (late, so that a CTA holds a unit in reserve only briefly:
+        // a reserved unit can leave other CTAs idle at the end), and its
+        // record is read and published three tiles later.  The producer runs
+        // stages ahead of the MMA, so neither latency reaches it, and the
+        // gather groups know the next unit before their last stage of this
+        // one and load its neuron ids while that stage lands.
+        const int kb_claim = U.kb > 10 ? U.kb - 10 : 0;
+        const int kb_read = U.kb > 7 ? U.kb - 7 : (U.kb > 1 ? 1 : 0);
+        int tk = 0;
+        if (U.kb == 0) Un = unit_of(atomicAdd(ticket, 1));
         for (int kb = 0; kb < U.kb; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u)) {
             { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
@@ -659,6 +720,15 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           if (++stage == UG_ST) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (kb == kb_claim) tk = atomicAdd(ticket, 1);
+          if (kb == kb_read) {
+            Un = unit_of(tk);
+            if (!publish(Un)) {
+              { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+              goto done;
+            }
+            published = true;
           }
         }
       }
@@ -672,10 +742,20 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const UgUnit U = Un;
-        if (u + static_cast<int>(gridDim.x) < num_units)
-          Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
+      int rs = 0;
+      uint32_t rph = 0;
+      for (;;) {
+        if (!ptx::mbar_wait(&rfull[rs], rph)) {
+          { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+          goto done;
+        }
+        const UgUnit U = ring[rs];
+        ptx::mbar_arrive(&rempty[rs]);
+        if (++rs == UG_RING) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        if (U.m < 0) break;
         if (U.kb == 0) continue;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
@@ -735,11 +815,48 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
     uint64_t* eb = &empty[grp];
     int seq = 0;
     int ids[32];
-    int ids_for = -1;  // up: the unit whose neuron ids are in ids[]
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const UgUnit U = Un;
-      if (u + static_cast<int>(gridDim.x) < num_units)
-        Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
+    int ids_for = -1;  // up: the unit (ring sequence number) whose neuron ids are in ids[]
+    int rs = 0;
+    uint32_t rph = 0;
+    int nu = 0;              // units taken from the ring
+    bool have_next = false;  // up: the next unit, taken early, is in Un
+    UgUnit Un{};
+    // the next unit from the ring (warp-uniform; false: the wait ran out)
+    auto take = [&](UgUnit& out) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&rfull[rs], rph))) return false;
+      out = ring[rs];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&rempty[rs]);
+      if (++rs == UG_RING) {
+        rs = 0;
+        rph ^= 1u;
+      }
+      ++nu;
+      return true;
+    };
+    // up: the next unit into Un and its neuron ids into ids[]
+    auto take_next = [&]() {
+      if (!take(Un)) return false;
+      have_next = true;
+      if (Un.m >= 0) {
+        const int32_t* Uln = p.Ulist + static_cast<size_t>(Un.m) * p.Fp;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ids[i] = __ldg(Uln + Un.j * 256 + (g >> 3) + 8 * i);
+        ids_for = nu;
+      }
+      return true;
+    };
+    for (;;) {
+      UgUnit U;
+      if (have_next) {
+        U = Un;
+        have_next = false;
+      } else if (!take(U)) {
+        if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+        goto done;
+      }
+      if (U.m < 0) break;
+      const int cur = nu;
       if (U.kb == 0) continue;
       const int32_t* Ul = p.Ulist + static_cast<size_t>(U.m) * p.Fp;
       // first K block of this unit that is this group's
@@ -776,7 +893,7 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
       int col = 0;
       uint32_t nbytes = 16;
       if (MODE == UG_UP) {
-        if (ids_for != u) {
+        if (ids_for != cur) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) ids[i] = __ldg(Ul + U.j * 256 + (g >> 3) + 8 * i);
         }
@@ -818,17 +935,23 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
           }
         }
         ptx::cp_async_commit();
-        if (MODE == UG_UP && kb + UG_ST >= U.kb && u + static_cast<int>(gridDim.x) < num_units) {
-          // the copies read their addresses at issue: load the next unit's
-          // ids now, while this stage lands
-          const int32_t* Uln = p.Ulist + static_cast<size_t>(Un.m) * p.Fp;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ids[i] = __ldg(Uln + Un.j * 256 + (g >> 3) + 8 * i);
-          ids_for = u + static_cast<int>(gridDim.x);
+        // This group's last stage of an up unit: the next unit's neuron ids
+        // are loaded while the stage lands (the copies read their addresses
+        // at issue) when the producer has already published that unit, else
+        // once the stage is marked full, before the group's next stage is free.
+        const bool last = MODE == UG_UP && kb + UG_ST >= U.kb;
+        const bool early = last && __all_sync(0xffffffffu, ptx::mbar_try_wait(&rfull[rs], rph));
+        if (early && !take_next()) {
+          if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+          goto done;
         }
         ptx::cp_async_wait<0>();
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(fb);
+        if (last && !early && !take_next()) {
+          if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+          goto done;
+        }
       }
     }
   } else {
@@ -838,10 +961,21 @@ __global__ void __launch_bounds__(UG_THREADS, 1)
     const int set = (warp - 2) >> 2;  // column half of the tile
     uint8_t* buf = smem + SM::STG + (warp - 2) * SM::STG_BUF;
     int local = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const UgUnit U = Un;
-      if (u + static_cast<int>(gridDim.x) < num_units)
-        Un = ug_unit<MODE>(p, u + static_cast<int>(gridDim.x));
+    int rs = 0;
+    uint32_t rph = 0;
+    for (;;) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&rfull[rs], rph))) {
+        if (lane == 0) { atomicOr(p.status, TWELL_FLAG_TIMEOUT); *aborted = 1u; }
+        goto done;
+      }
+      const UgUnit U = ring[rs];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&rempty[rs]);
+      if (++rs == UG_RING) {
+        rs = 0;
+        rph ^= 1u;
+      }
+      if (U.m < 0) break;
       const int pos = U.m * UG_BM + r;  // position of this row
       const bool valid = pos < p.T;
       const int t = !valid ? 0
