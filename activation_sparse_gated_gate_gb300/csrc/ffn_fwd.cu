@@ -354,7 +354,7 @@ twell_status launch_nc(FfnParams p, const DeviceInfo& dev, cudaStream_t s) {
   }
   p.upr = (p.n_t + p.G - 1) / p.G;
   p.split = p.upr > 1;
-  if (p.split &&
+  if (p.split && !p.y_zeroed &&
       cudaMemsetAsync(p.y, 0, static_cast<size_t>(p.T) * p.D * sizeof(float), s) != cudaSuccess)
     return TWELL_ERR_CUDA;
   const long long units = static_cast<long long>(p.T) * p.upr;
@@ -394,7 +394,15 @@ twell_status launch_fused(const FfnParams& p, const DeviceInfo& dev, cudaStream_
 extern "C" twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
                                       const uint16_t* Wd, int32_t D, float* y,
                                       int32_t* status_dev, void* stream) {
-  using namespace twell;
+  return twell::ffn_fwd_twell(x, h, Wu_t, Wd, D, y, status_dev,
+                              static_cast<cudaStream_t>(stream), false);
+}
+
+namespace twell {
+
+twell_status ffn_fwd_twell(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
+                           const uint16_t* Wd, int32_t D, float* y, int32_t* status_dev,
+                           cudaStream_t stream, bool y_zeroed) {
   if (h == nullptr) return TWELL_ERR_INVALID;
   const int32_t T = h->T, F = h->F;
   if (T < 0 || F <= 0 || F % TWELL_TILE != 0 || D <= 0 || D % 8 != 0) return TWELL_ERR_INVALID;
@@ -427,5 +435,8 @@ extern "C" twell_status twell_ffn_fwd(const uint16_t* x, const twell_t* h, const
   p.n_rows = nullptr;
   p.ell_rows = nullptr;
   p.u_save = nullptr;
-  return launch_fused(p, dev, static_cast<cudaStream_t>(stream), false);
+  p.y_zeroed = y_zeroed ? 1 : 0;
+  return launch_fused(p, dev, stream, false);
 }
+
+}  // namespace twell

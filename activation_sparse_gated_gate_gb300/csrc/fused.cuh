@@ -29,6 +29,8 @@ struct FfnParams {
   const int32_t* n_rows;
   const int32_t* ell_rows;
   float* u_save;
+  // y is zero on the stream already (split rows then skip their memset)
+  int32_t y_zeroed;
 };
 
 struct Entry {
@@ -40,6 +42,13 @@ struct Entry {
 // Launch the fused up+down kernel: TwELL rows (ell = false) or the ELL rows
 // of a hybrid (ell = true; n_rows / ell_rows / u_save set, W = C, no spill).
 twell_status launch_fused(const FfnParams& p, const DeviceInfo& dev, cudaStream_t s, bool ell);
+
+// twell_ffn_fwd with its arguments already checked by the caller except the
+// TwELL's; `y_zeroed`: y [T][D] is zero on `s` already (the decode step's
+// gate kernel zeroes it), so no memset precedes the kernel.
+twell_status ffn_fwd_twell(const uint16_t* x, const twell_t* h, const uint16_t* Wu_t,
+                           const uint16_t* Wd, int32_t D, float* y, int32_t* status_dev,
+                           cudaStream_t s, bool y_zeroed);
 
 // Workspace bytes of twell_ffn_fwd_tc (sorted: twell_ffn_fwd_tc_sorted) for T
 // rows, width D and F gate columns.

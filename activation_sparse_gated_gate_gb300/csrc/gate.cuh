@@ -18,6 +18,9 @@ struct DecodeFfn {
   const uint16_t* Wu_t;  // [F][D] bf16
   const uint16_t* Wd;    // [F][D] bf16
   float* y;
+  // with y NULL: [T][D] fp32 the kernel zeroes (NULL: none) for the forward
+  // that follows, which adds into it
+  float* y_zero;
 };
 
 // Enqueue the decode-size gate kernel (the caller has validated the

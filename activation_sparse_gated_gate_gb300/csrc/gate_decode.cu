@@ -95,6 +95,7 @@ struct DecParams {
   const uint16_t* Wu_t;
   const uint16_t* Wd;
   float* y;
+  float* y_zero;      // prefetch mode: y of the forward that follows, zeroed here
 };
 
 __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
@@ -249,8 +250,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (ok) ptx::mma_commit(tfull);
     }
   } else {
-    // epilogue warps: the accumulator is complete (the decision is
-    // warp-uniform; tcgen05.ld below is warp-collective)
+    // epilogue warps: first, in prefetch mode, zero this CTA's share of the
+    // forward's y while W_g streams (the forward adds into y); then wait
+    // until the accumulator is complete (the decision is warp-uniform;
+    // tcgen05.ld below is warp-collective)
+    if (p.y_zero) {
+      const size_t n4 = static_cast<size_t>(p.T) * p.D / 4;
+      float4* y4 = reinterpret_cast<float4*>(p.y_zero);
+      const size_t nthr = static_cast<size_t>(gridDim.x) * (kThreads - 64);
+      for (size_t i = static_cast<size_t>(blockIdx.x) * (kThreads - 64) + (threadIdx.x - 64);
+           i < n4; i += nthr)
+        y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (!__all_sync(0xffffffffu, pipe_wait(tfull, 0, p.wait_ns)) && lane == 0) {
       flag(p.status, TWELL_FLAG_TIMEOUT);
       *aborted = 1u;
@@ -563,6 +574,7 @@ twell_status launch_gate_decode(const DeviceInfo& dev, const uint16_t* x, const 
   p.Wu_t = ffn ? ffn->Wu_t : nullptr;
   p.Wd = ffn ? ffn->Wd : nullptr;
   p.y = ffn ? ffn->y : nullptr;
+  p.y_zero = ffn && !ffn->y ? ffn->y_zero : nullptr;
 
   CUtensorMap mx, mw;
   twell_status st;

@@ -33,6 +33,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "fused.cuh"
 #include "gate.cuh"
 #include "ptx.cuh"
 
@@ -465,15 +466,16 @@ extern "C" twell_status twell_ffn_decode(const uint16_t* x, const uint16_t* Wg_t
   if (T <= kDecodeProjectMaxT || D > kFusedMaxD) {
     if (cudaMemsetAsync(y, 0, static_cast<size_t>(T) * D * sizeof(float), s) != cudaSuccess)
       return TWELL_ERR_CUDA;
-    const DecodeFfn ffn{Wu_t, Wd, y};
+    const DecodeFfn ffn{Wu_t, Wd, y, nullptr};
     return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, wait_ns, &ffn,
                               s);
   }
-  const DecodeFfn prefetch{Wu_t, Wd, nullptr};
+  // (the gate kernel also zeroes y for the forward, which adds into it)
+  const DecodeFfn prefetch{Wu_t, Wd, nullptr, y};
   if ((st = launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, wait_ns,
                                &prefetch, s)) != TWELL_OK)
     return st;
-  return twell_ffn_fwd(x, out, Wu_t, Wd, D, y, status_dev, stream);
+  return ffn_fwd_twell(x, out, Wu_t, Wd, D, y, status_dev, s, true);
 }
 
 extern "C" uint64_t twell_gate_pack_wait_limit(uint64_t ns) {

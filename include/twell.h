@@ -140,9 +140,10 @@ twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t, int32_t T,
  * active entry of z -- slots and spill alike, so nothing is dropped when the
  * spill list is full -- adds its row to y with fp32 atomics.  With more
  * tokens the gate kernel prefetches the active neurons' W_u and W_d rows
- * into L2 while it packs, and the call then runs twell_ffn_fwd on the TwELL
- * it wrote (whose rules then hold: a missing spill slice is skipped and
- * flagged).  Rows with no active entry get y_t = 0.
+ * into L2 and zeroes y while it streams W_g, and the call then runs
+ * twell_ffn_fwd's kernel on the TwELL it wrote (whose rules then hold: a
+ * missing spill slice is skipped and flagged).  Rows with no active entry
+ * get y_t = 0.
  *   x   [T][D] bf16   Wg_t, Wu_t, Wd  [F][D] bf16   y  [T][D] fp32 (written;
  *   zeroed by the call, stream-ordered)   status_dev  device int32 (required)
  * Supports 1 <= T <= 256 with D > 64 (TWELL_ERR_UNSUPPORTED otherwise:

@@ -113,6 +113,28 @@ def test_all_active_equals_dense_library_gemm():
     check_y(y.cpu().numpy().astype(np.float64), w, z.cpu().numpy())
 
 
+@pytest.mark.parametrize("T", [64, 300])  # decode-size and batch gate kernels
+def test_spill_count_between_packs(T):
+    """Packs that spill, then none, then again, into one TwELL (through
+    twell_gate_pack and, at decode sizes, twell_ffn_decode) each report
+    their own spill count: the count starts from zero on every call."""
+    heavy = workloads.random_small(T, 256, 1024, 0.4, 4, seed=T + 11)
+    light = workloads.random_small(T, 256, 1024, 0.004, 4, seed=T + 12)
+    dh, dl = upload(heavy), upload(light)
+    h = tw.TwELL(T, 1024, 4)
+    calls = [lambda d: tw.twell_gate_pack(d["x"], d["Wg_t"], h)]
+    if T <= 256:
+        calls.append(lambda d: tw.twell_ffn_decode(d["x"], d["Wg_t"], d["Wu_t"], d["Wd"], h))
+    for call in calls:
+        for d in (dh, dl, dh, dl):
+            call(d)
+            torch.cuda.synchronize()
+            expect = int((h.cnt.cpu().numpy() > 4).sum())
+            assert int(h.spill_n.item()) == expect
+            assert expect > 0 if d is dh else True
+    assert int(h.status.item()) == 0
+
+
 def test_spill_capacity_exhausted_sets_flag():
     w = workloads.random_small(64, 128, 1024, 0.5, 8, seed=5)
     d, h, z = run_pack(w, spill_cap=4)
