@@ -61,22 +61,22 @@ METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of ro
 TRAFFIC = {
     # 1.5B-class layer (profiles/ffn_fwd_tc_1.5B_T16384.md)
     ("twell_ffn_fwd_tc_sorted", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        749.93e6, "csrc/ffn_tc.cu", "ce774a5060b43d46", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        789.88e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        788.75e6, "csrc/ffn_tc.cu", "ce774a5060b43d46", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        818.67e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        776.39e6, "csrc/ffn_fwd.cu", "69ac3bf21e44a5d5", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        776.28e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        149.93e6, "csrc/gate_pack.cu", "d2486faee81ad268", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        149.63e6, "csrc/gate_pack.cu", "3681f4f55da01706", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        212.53e6, "csrc/ffn_tc.cu", "ce774a5060b43d46", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        220.69e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc_sorted", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        239.57e6, "csrc/ffn_tc.cu", "ce774a5060b43d46", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        246.90e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        105.84e6, "csrc/ffn_fwd.cu", "69ac3bf21e44a5d5", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        106.01e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        45.02e6, "csrc/gate_pack.cu", "d2486faee81ad268", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        45.04e6, "csrc/gate_pack.cu", "3681f4f55da01706", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
 
 
