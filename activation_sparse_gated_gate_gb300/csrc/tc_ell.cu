@@ -35,6 +35,7 @@
 // their completion barrier may no longer complete once another role left).
 #include <cuda_fp16.h>
 
+#include "gemm.cuh"
 #include "ptx.cuh"
 #include "scale.cuh"
 #include "bounds.cuh"
@@ -77,16 +78,24 @@ __device__ __forceinline__ uint16_t f16_bits(float v, int32_t* status) {
 // Per-unit decomposition shared by every role.  Returns 0 (nothing to do),
 // 1 (a tile with K blocks [kb0, kb1)) or 2 (a TRANS tile with an empty K
 // range: its output is zero).
+// With ks = 2 K parts per tile, unit u is part u % 2 of tile u / 2; the parts
+// split the K blocks in halves (ROWS: at an even block, as a raw ELL slot
+// covers two) and one of them may be empty.
 struct Units {
   int num_m, num_n, total_kb, kb_per_seg;
   int n_rows;
+  int ks;
   __device__ int info(int u, int mode, int& m_blk, int& n_blk, int& kb0, int& kb1) const {
-    m_blk = u / num_n;
-    n_blk = u % num_n;
-    kb0 = 0;
-    kb1 = total_kb;
+    const int t = u / ks, part = u - t * ks;
+    m_blk = t / num_n;
+    n_blk = t % num_n;
+    int mid = total_kb / 2;
+    if (mode == TC_ROWS) mid &= ~1;
+    kb0 = ks == 1 || part == 0 ? 0 : mid;
+    kb1 = ks == 1 || part == 1 ? total_kb : mid;
     if (mode != TC_TRANS && m_blk * BM >= n_rows) return 0;
-    return total_kb > 0 ? 1 : (mode == TC_TRANS ? 2 : 0);
+    if (total_kb == 0) return mode == TC_TRANS ? 2 : 0;
+    return kb1 > kb0 ? 1 : 0;
   }
 };
 
@@ -119,6 +128,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
   U.num_m = num_m;
   U.num_n = num_n;
   U.n_rows = min(*p.n_rows, p.rows_cap);
+  U.ks = p.ksplit > 1 ? 2 : 1;
   if (MODE == TC_ROWS) {
     U.kb_per_seg = p.F / BK;
     U.total_kb = p.nseg * U.kb_per_seg;
@@ -129,7 +139,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
     U.kb_per_seg = p.D / BK;
     U.total_kb = p.nseg * U.kb_per_seg;
   }
-  const int num_units = num_m * num_n;
+  const int num_units = num_m * num_n * U.ks;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -536,11 +546,18 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
           if (valid) {
             float4* o4 = reinterpret_cast<float4*>(o + c * 32);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              o4[j] = make_float4(osc * __uint_as_float(v[4 * j]),
-                                  osc * __uint_as_float(v[4 * j + 1]),
-                                  osc * __uint_as_float(v[4 * j + 2]),
-                                  osc * __uint_as_float(v[4 * j + 3]));
+            for (int j = 0; j < 8; ++j) {
+              const float4 q = make_float4(osc * __uint_as_float(v[4 * j]),
+                                           osc * __uint_as_float(v[4 * j + 1]),
+                                           osc * __uint_as_float(v[4 * j + 2]),
+                                           osc * __uint_as_float(v[4 * j + 3]));
+              // two K parts add into the zeroed output: 0 + a + b is the same
+              // sum in either order, so repeats stay bit-identical
+              if (U.ks > 1)
+                atomicAdd(o4 + j, q);
+              else
+                o4[j] = q;
+            }
           }
         }
       }
@@ -584,10 +601,32 @@ twell_status tc_launch(const TcMaps& maps, const TcArgs& a, const DeviceInfo& de
     return TWELL_ERR_CUDA;
   const int num_m = MODE == TC_TRANS ? a.F / BM : (a.rows_cap + BM - 1) / BM;
   const int num_n = MODE <= TC_SAMPLE_DA ? (a.F + BN - 1) / BN : (a.D + BN - 1) / BN;
-  const long long units = static_cast<long long>(num_m) * num_n;
+  long long units = static_cast<long long>(num_m) * num_n;
   if (units == 0) return TWELL_OK;
+  // TRANS, and ROWS over several segments, with fewer than eight tiles per
+  // SM: two K parts per tile, so the last, partial round of tiles costs half
+  // a tile, for a zeroed output and atomic additions.  Measured at the
+  // 2B-class layer (648 TRANS tiles, 1125 ROWS tiles on 152 SMs): backward
+  // 5.16 -> 5.03 ms; the forward's one-segment ROWS lost more to the zeroing
+  // and the atomics than it gained (1.31 -> 1.33 ms), so it keeps one part.
+  TcArgs ak = a;
+  ak.ksplit = 1;
+  if (!Cfg::SAMPLE && (MODE == TC_TRANS || a.nseg > 1) && units < 8LL * dev.sm_count) {
+    ak.ksplit = 2;
+    units *= 2;
+    if (MODE == TC_TRANS) {
+      if (cudaMemset2DAsync(a.out, static_cast<size_t>(a.ldo) * 4, 0,
+                            static_cast<size_t>(a.D) * 4, static_cast<size_t>(a.F), s) !=
+          cudaSuccess)
+        return TWELL_ERR_CUDA;
+    } else {
+      twell_status st = zero_rows(a.out, a.ldo, a.row_idx, a.rows_cap, a.n_rows, a.D, s,
+                                  a.row_limit, a.status);
+      if (st != TWELL_OK) return st;
+    }
+  }
   const int grid = static_cast<int>(units < dev.sm_count ? units : dev.sm_count);
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(maps, a, num_m, num_n);
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(maps, ak, num_m, num_n);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

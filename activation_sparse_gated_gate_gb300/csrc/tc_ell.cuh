@@ -75,6 +75,9 @@ struct TcArgs {
   const int32_t* row_idx;  // ROWS: output row of ELL row i
   int32_t row_limit;       // rows of out that row_idx may name (0: unchecked)
   int32_t* status;
+  // ROWS / TRANS, set by the launch: K parts per tile (1 or 2); with 2, each
+  // part adds its product into out, which the launch zeroes first
+  int32_t ksplit;
 };
 
 // Tensor maps of the operands (box shapes as listed in TcMaps).
