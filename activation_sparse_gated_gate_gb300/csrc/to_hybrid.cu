@@ -12,7 +12,8 @@
 //             dense_rows, n_ell, n_dense (deterministic)
 //   ell_fill  one warp per ELL row (grid sized by T, rows past n_ell exit):
 //             lane k copies tile k's count and entries (slots, or the spill
-//             slice when W < count <= C)
+//             slice when W < count <= C); with W == C (16 or 32) whole
+//             16-byte chunks of slots instead (ell_copy)
 //   dense_fill one CTA per dense row: thread j writes ReLU(z) of column j
 //             from the slots or the spill slice (coalesced row writes)
 #include "bounds.cuh"
@@ -153,6 +154,50 @@ __global__ void __launch_bounds__(256) ell_fill_kernel(const HybParams p) {
   }
 }
 
+// ell_fill for W == C (16 or 32) and 16-byte aligned slot arrays, the
+// training setting, where a tile's slots are its ELL entries: whole 16-byte
+// chunks instead of one slot at a time.  One warp per ELL row, a group of
+// eight lanes per tile, four tiles at a time: lane j copies value chunk j
+// (slots 4j .. 4j+3) when it holds entries, and lanes j < C / 16 write column
+// chunk j with the slots at and past the count set to the padding sentinel.
+template <int C>
+__global__ void __launch_bounds__(256) ell_copy_kernel(const HybParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (i >= *p.n_ell) return;
+  const int t = p.ell_rows[i];
+  if (!in_bounds(t, p.T, p.status)) return;  // warp-uniform
+  const size_t src_rt = static_cast<size_t>(t) * p.n_t;
+  const size_t dst_rt = static_cast<size_t>(i) * p.n_t;
+  const int j = lane & 7;
+  for (int k = lane >> 3; k < p.n_t; k += 4) {
+    const int c = min(static_cast<int>(p.cnt[src_rt + k]), C);  // <= C for an ELL row
+    if (j < C / 4 && 4 * j < c)
+      reinterpret_cast<uint4*>(p.ell_val + (dst_rt + k) * C)[j] =
+          __ldg(reinterpret_cast<const uint4*>(p.val + (src_rt + k) * C) + j);
+    if (j < C / 16) {
+      const uint4 w = 16 * j < c
+                          ? __ldg(reinterpret_cast<const uint4*>(p.col + (src_rt + k) * C) + j)
+                          : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t o[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t r = 0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int slot = 16 * j + 4 * q + b;
+          const uint32_t v = slot < c ? (static_cast<uint32_t>(tile_col((o[q] >> (8 * b)) & 0xffu)) & 0xffu)
+                                      : 0xffu;
+          r |= v << (8 * b);
+        }
+        o[q] = r;
+      }
+      reinterpret_cast<uint4*>(p.ell_col + (dst_rt + k) * C)[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (j == 0) p.ell_cnt[dst_rt + k] = static_cast<uint8_t>(c);
+  }
+}
+
 __global__ void __launch_bounds__(256) dense_fill_kernel(const HybParams p) {
   const int i = blockIdx.x;
   const int n = min(*p.n_dense, p.max_dense);
@@ -240,7 +285,13 @@ extern "C" twell_status twell_to_hybrid(const twell_t* h, const hybrid_t* out,
   const int warp_blocks = static_cast<int>((static_cast<long long>(p.T) * 32 + 255) / 256);
   classify_kernel<<<warp_blocks, 256, 0, s>>>(p);
   scan_kernel<<<1, kScanThreads, 0, s>>>(p);
-  ell_fill_kernel<<<warp_blocks, 256, 0, s>>>(p);
+  const bool chunks = p.W == p.C && aligned16(h->val) && aligned16(h->col);
+  if (chunks && p.C == 32)
+    ell_copy_kernel<32><<<warp_blocks, 256, 0, s>>>(p);
+  else if (chunks && p.C == 16)
+    ell_copy_kernel<16><<<warp_blocks, 256, 0, s>>>(p);
+  else
+    ell_fill_kernel<<<warp_blocks, 256, 0, s>>>(p);
   if (p.max_dense > 0) dense_fill_kernel<<<p.max_dense, 256, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

@@ -50,6 +50,8 @@ def _assert_hybrid_equal(hyb, ref, max_dense):
 
 @pytest.mark.parametrize("T,D,F,p,W,cap", [
     (300, 128, 1024, 0.05, 8, 8),      # C == W
+    (300, 128, 1024, 0.06, 16, 16),    # C == W = 16: whole 16-byte chunks of slots
+    (211, 128, 1280, 0.12, 32, 32),    # C == W = 32 (the training width), ragged T
     (257, 64, 512, 0.10, 8, 16),       # C > W: ELL entries from spill slices
     (200, 128, 640, 0.10, 16, 8),      # C < W
     (64, 64, 256, 0.001, 8, 8),        # almost nothing active
