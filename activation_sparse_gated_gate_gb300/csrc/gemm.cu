@@ -229,7 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     kb_seg[s] = len > 0 ? (len + BK - 1) / BK : 0;
     total_kb += kb_seg[s];
   }
-  const int num_tiles = num_m * num_n;
+  // only the row tiles that hold rows of this call: with the row count a
+  // device value (overflow rows) the launch covers the maximum, and a unit
+  // numbering over all of them left whole CTAs without work (152 CTAs and 8
+  // row tiles of which 4 were present: every CTA's units fell in the same row
+  // tile, so half the SMs sat idle)
+  const int num_m_act = min(num_m, (M_act + BM - 1) / BM);
+  const int num_tiles = num_m_act * num_n;
   const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
   const int num_units = num_tiles * ksplit;
   const int kb_chunk = (total_kb + ksplit - 1) / ksplit;
@@ -237,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto unit_range = [&](int u, int& m_blk, int& n_blk, int& kb0, int& kb1) {
     const int tile = u % num_tiles;
     const int ks = u / num_tiles;
-    m_blk = tile % num_m;
-    n_blk = tile / num_m;
+    m_blk = tile % num_m_act;
+    n_blk = tile / num_m_act;
     kb0 = ks * kb_chunk;
     kb1 = min(total_kb, kb0 + kb_chunk);
     return m_blk * BM < M_act && kb0 < kb1;
