@@ -49,6 +49,7 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 // at T = 1 and 4 and ties at 16), and for rows wider than the CUDA-core fused
 // kernel takes
 constexpr int32_t kDecodeProjectMaxT = 8;
+constexpr int32_t kGateDecodeMaxT = 192;  // twell_gate_pack: the decode kernel up to here
 constexpr int32_t kFusedMaxD = 256 * 12;
 
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -415,8 +416,11 @@ extern "C" twell_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg_t,
 
   // Decode-sized batches: the split-K kernel with the tokens as the MMA's N
   // (every TwELL tile on a 2-CTA cluster, W_g streamed once; it stores every
-  // block-bitmap word itself).
-  if (gate_decode_supported(T, D))
+  // block-bitmap word itself).  Above 192 tokens its packing epilogue (16
+  // tokens per step and set) outweighs the stream, and the batch kernel is
+  // the faster (d_model 2048, d_ff 8192, graph replay: 23.7 against 25.7 us
+  // at T = 224 and 256, equal at 128-192, 19.6 against 21.6 us at T = 96).
+  if (gate_decode_supported(T, D) && T <= kGateDecodeMaxT)
     return launch_gate_decode(dev, x, Wg_t, T, D, F, out, z_debug, status_dev, p.wait_ns,
                               nullptr, s);
 

@@ -67,7 +67,7 @@ TRAFFIC = {
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
         776.28e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        149.63e6, "csrc/gate_pack.cu", "3681f4f55da01706", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        149.95e6, "csrc/gate_pack.cu", "541fa10f1d139aef", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         220.69e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
@@ -76,7 +76,7 @@ TRAFFIC = {
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         106.01e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        45.04e6, "csrc/gate_pack.cu", "3681f4f55da01706", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        45.03e6, "csrc/gate_pack.cu", "541fa10f1d139aef", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
 
 
