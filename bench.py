@@ -819,6 +819,63 @@ def infer_entry(args, case, flush, peaks, fma, steps, warmup, forward="auto", cl
                    "union_sum": union_sum}
 
 
+def layer_stack(case, flush, steps, warmup, peaks, fma, nnz, n_active, layers=8):
+    """The decode step as a decoding loop runs it: `layers` layers, each with
+    weights of its own, in one CUDA graph.  Layer l's W_g, W_u and W_d are
+    layer 0's with the neurons permuted (the same computation and the same
+    active counts, in other memory); the layers' weights (about 100 MB each
+    at d_model 2048, d_ff 8192) together exceed L2 several times, so every
+    layer reads them from DRAM, with one L2 flush per replay.  Per-layer time
+    = the graph's time / layers: the graph's own launch cost (several
+    microseconds, paid once per replay) no longer lands on a single layer."""
+    import torch
+    import activation_sparse_gated_gate_gb300 as tw
+    w, dev = case.w, case.dev
+    hbm, bf16, _, _ = peaks
+    gen = torch.Generator().manual_seed(2024)
+    lay = []
+    for l in range(layers):
+        if l == 0:
+            Wg, Wu, Wd = case.Wg, case.Wu, case.Wd
+        else:
+            perm = torch.randperm(w.F, generator=gen).to(dev)
+            Wg, Wu, Wd = (case.Wg[perm].contiguous(), case.Wu[perm].contiguous(),
+                          case.Wd[perm].contiguous())
+        lay.append((Wg, Wu, Wd, tw.TwELL(w.T, w.F, w.width, device=dev),
+                    torch.empty((w.T, w.D), dtype=torch.float32, device=dev)))
+
+    def run(st):
+        for Wg, Wu, Wd, h, y in lay:
+            tw.twell_ffn_decode(case.x, Wg, Wu, Wd, h, y=y, stream=st)
+
+    graph = _capture(dev, run)
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record(case.stream)
+        graph.replay()
+        e[1].record(case.stream)
+    torch.cuda.synchronize()
+    if any(int(h.status.item()) for _, _, _, h, _ in lay):
+        raise RuntimeError(f"device status flags in the layer stack ({w.name})")
+    # the same y in every layer (a permutation of the neurons changes no sum's terms)
+    rel = float((lay[-1][4] - lay[0][4]).norm() / max(float(lay[0][4].norm()), 1e-30))
+    if not rel < 1e-4:
+        raise RuntimeError(f"layer stack: permuted layers differ ({rel:.2e}, {w.name})")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / layers
+    r = decode_roofline(w.T, w.D, w.F, nnz, n_active, ms, hbm, fma, bf16)
+    return {"layers": layers, "ms_per_layer": ms,
+            "tokens_per_s_per_layer": job_tokens_per_s(w.T, int(os.environ.get("WORLD_SIZE", "1")), ms),
+            "hbm_frac": r["hbm"]["frac"], "binding": r["binding"],
+            "how": ("twell_ffn_decode for each of the layers in one CUDA graph, one L2 flush per "
+                    "replay (the layers' weights exceed L2); layer l's weights are layer 0's with "
+                    "the neurons permuted; time per layer = graph time / layers")}
+
+
 def headline_roofline(entry, raw, peaks, fma_meta):
     """The `roofline` object of the JSON line: the step's dominant kernel
     against its binding roofline, with the HBM view and (for the tensor-core
@@ -1325,6 +1382,9 @@ def run_ours(args, head_cfg):
             e, r = infer_entry(args, cc, flush, peaks, fma, max(K, 10), args.warmup,
                                args.forward)
             e["roofline"] = headline_roofline(e, r, peaks, fma_meta)
+            if c == 4:
+                e["layer_stack"] = layer_stack(cc, flush, max(K, 10), args.warmup, peaks, fma,
+                                               r["nnz"], r["n_active"])
             configs[wc.name] = e
             del cc
             torch.cuda.empty_cache()
