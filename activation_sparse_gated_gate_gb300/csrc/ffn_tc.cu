@@ -271,7 +271,17 @@ __global__ void __launch_bounds__(UG_SORT_THREADS) ug_key_kernel(const UgArgs p)
   if (t < p.T) {
     const uint8_t* row = p.cnt + static_cast<size_t>(t) * p.n_t;
     int n = 0;
-    if ((p.n_t & 3) == 0) {
+    if ((p.n_t & 15) == 0 && (reinterpret_cast<uintptr_t>(p.cnt) & 15) == 0) {
+      for (int k = 0; k < p.n_t; k += 16) {
+        const uint4 w4 = __ldg(reinterpret_cast<const uint4*>(row + k));
+        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t s2 = (ws[e] & 0x00ff00ffu) + ((ws[e] >> 8) & 0x00ff00ffu);
+          n += static_cast<int>((s2 & 0xffffu) + (s2 >> 16));
+        }
+      }
+    } else if ((p.n_t & 3) == 0) {
       for (int k = 0; k < p.n_t; k += 4) {
         const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(row + k));
         const uint32_t s2 = (w & 0x00ff00ffu) + ((w >> 8) & 0x00ff00ffu);
@@ -364,15 +374,29 @@ __global__ void __launch_bounds__(UG_PREP_THREADS) ug_bits_kernel(const UgArgs p
   for (int i = threadIdx.x; i < nw; i += UG_PREP_THREADS) bm[i] = 0u;
   if (p.xp) {
     // sorted order: the CTA's positions' x rows, xp[i] = x[perm[i]], for the
-    // up GEMM's TMA tiles (16-byte steps; bandwidth-bound, it overlaps the
-    // latency-bound walk below across the CTAs of an SM)
+    // up GEMM's TMA tiles (16-byte steps, four loads in flight per thread
+    // before their stores; bandwidth-bound, it overlaps the latency-bound
+    // walk below across the CTAs of an SM)
+    constexpr int kInFlight = 4;
     const int per_row = p.D / 8;
-    for (int i = threadIdx.x; i < rows * per_row; i += UG_PREP_THREADS) {
-      const int r = i / per_row;
-      const int q = i - r * per_row;
-      const int t = static_cast<int>(clamp_index(p.perm[r0 + r], p.T, p.status));
-      reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(r0 + r) * p.D)[q] =
-          __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.D) + q);
+    const int n = rows * per_row;
+    uint4* xp4 = reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(r0) * p.D);
+    for (int i0 = threadIdx.x; i0 < n; i0 += kInFlight * UG_PREP_THREADS) {
+      uint4 v[kInFlight];
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u) {
+        const int i = i0 + u * UG_PREP_THREADS;
+        if (i < n) {
+          const int r = i / per_row;
+          const int t = static_cast<int>(clamp_index(p.perm[r0 + r], p.T, p.status));
+          v[u] = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.D) +
+                       (i - r * per_row));
+        }
+      }
+      // rows r0.. of xp are contiguous: position i of the CTA's rows is xp4[i]
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u)
+        if (i0 + u * UG_PREP_THREADS < n) xp4[i0 + u * UG_PREP_THREADS] = v[u];
     }
   }
   __syncthreads();

@@ -61,18 +61,18 @@ METRIC = "sparse gated-FFN tokens/s per layer (fwd; fwd+bwd) on 1 GB300, % of ro
 TRAFFIC = {
     # 1.5B-class layer (profiles/ffn_fwd_tc_1.5B_T16384.md)
     ("twell_ffn_fwd_tc_sorted", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        789.88e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        780.73e6, "csrc/ffn_tc.cu", "e9eb6d8e73758029", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        818.67e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        828.30e6, "csrc/ffn_tc.cu", "e9eb6d8e73758029", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
         776.28e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
         149.95e6, "csrc/gate_pack.cu", "541fa10f1d139aef", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
     ("twell_ffn_fwd_tc", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        220.69e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        219.47e6, "csrc/ffn_tc.cu", "e9eb6d8e73758029", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd_tc_sorted", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        246.90e6, "csrc/ffn_tc.cu", "f6b4b38f1ce049e3", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        246.89e6, "csrc/ffn_tc.cu", "e9eb6d8e73758029", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         106.01e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
