@@ -65,7 +65,7 @@ TRAFFIC = {
     ("twell_ffn_fwd_tc", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
         828.30e6, "csrc/ffn_tc.cu", "e9eb6d8e73758029", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
-        776.28e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        775.65e6, "csrc/ffn_fwd.cu", "2e583b71ad421583", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "1.5B-class T=16384 D=2048 F=8192 mean 1% heavy-tail W=16"): (
         149.95e6, "csrc/gate_pack.cu", "541fa10f1d139aef", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     # 0.5B-class layer (the same profile, second table)
@@ -74,7 +74,7 @@ TRAFFIC = {
     ("twell_ffn_fwd_tc_sorted", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         246.89e6, "csrc/ffn_tc.cu", "e9eb6d8e73758029", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_ffn_fwd", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
-        106.01e6, "csrc/ffn_fwd.cu", "a91fd166df282f4d", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
+        105.89e6, "csrc/ffn_fwd.cu", "2e583b71ad421583", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
     ("twell_gate_pack", "0.5B-class T=8192 D=1536 F=6144 1% W=8"): (
         45.03e6, "csrc/gate_pack.cu", "541fa10f1d139aef", "profiles/ffn_fwd_tc_1.5B_T16384.md"),
 }
